@@ -1,0 +1,147 @@
+"""CPU oracle for MoE layout / dispatch / combine (test infrastructure).
+
+Only the tests, the package smoke check and the benchmark's CPU-baseline leg
+may import this module.  The library itself never does: its product path is
+the CUDA library alone.
+
+The arithmetic lives in plain C (moedc_oracle.c, compiled without fused
+multiply-add or fast-math); this file builds it with gcc and wraps it with
+ctypes over numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moedc_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libmoedc_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+ERR_CAPACITY = 2
+ERR_EXPERT_RANGE = 3
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc; returns the library path."""
+    with _lock:
+        if not force and os.path.exists(_LIB_PATH) and \
+                os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+            return _LIB_PATH
+        os.makedirs(_OUT_DIR, exist_ok=True)
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    I64 = ctypes.c_int64
+    lib.oracle_layout.argtypes = [P, I, I, I, I, I, P, P, P, P]
+    lib.oracle_layout.restype = I
+    lib.oracle_dispatch.argtypes = [P, I, I, P, P, I, I, I, I, P, P, P]
+    lib.oracle_dispatch.restype = I
+    lib.oracle_combine.argtypes = [P, I, I, I, P, P, P, I, I, P]
+    lib.oracle_combine.restype = I
+    lib.oracle_e4m3_encode_n.argtypes = [P, P, I64]
+    lib.oracle_e4m3_decode_n.argtypes = [P, P, I64]
+    lib.oracle_f32_to_bf16_n.argtypes = [P, P, I64]
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e4m3_encode_n(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def e4m3_decode(c: np.ndarray) -> np.ndarray:
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.empty(c.shape, np.float32)
+    _load().oracle_e4m3_decode_n(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def f32_to_bf16(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_f32_to_bf16_n(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def bf16_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def layout(topk_idx: np.ndarray, E: int, R: int, cap: int) -> dict:
+    """Returns counts, rank counts, token-in-rank mask, slot map and status."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, K = topk_idx.shape
+    out = dict(
+        num_tokens_per_expert=np.empty(E, np.int32),
+        num_tokens_per_rank=np.empty(R, np.int32),
+        is_token_in_rank=np.empty((T, R), np.uint8),
+        slot=np.empty((T, K), np.int32),
+    )
+    out["status"] = _load().oracle_layout(
+        _ptr(topk_idx), T, K, E, R, cap, _ptr(out["num_tokens_per_expert"]),
+        _ptr(out["num_tokens_per_rank"]), _ptr(out["is_token_in_rank"]), _ptr(out["slot"]))
+    return out
+
+
+def dispatch(x: np.ndarray, topk_idx: np.ndarray, slot: np.ndarray, E: int, cap: int,
+             fp8: bool, recv: np.ndarray | None = None) -> dict:
+    """x: uint16 bf16 bits [T, H].  Returns recv ([E,cap,H] uint16 or uint8),
+    scales ([E,cap,H/128] float32, fp8 only), src_idx and status.
+    Rows no entry reaches keep their initial contents (zeros unless `recv`
+    is given)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    T, H = x.shape
+    K = topk_idx.shape[1] if topk_idx.ndim == 2 else 0
+    if recv is None:
+        recv = np.zeros((E, cap, H), np.uint8 if fp8 else np.uint16)
+    scales = np.zeros((E, cap, H // 128), np.float32) if fp8 else np.zeros(1, np.float32)
+    src_idx = np.empty((E, cap), np.int32)
+    status = _load().oracle_dispatch(_ptr(x), T, H, _ptr(topk_idx), _ptr(slot), K, E, cap,
+                                     1 if fp8 else 0, _ptr(recv), _ptr(scales), _ptr(src_idx))
+    return dict(recv=recv, scales=scales if fp8 else None, src_idx=src_idx, status=status)
+
+
+def combine(expert_out: np.ndarray, topk_idx: np.ndarray, slot: np.ndarray,
+            topk_weights: np.ndarray) -> dict:
+    """expert_out: uint16 bf16 bits [E, cap, H].  Returns y (uint16 [T, H]) and status."""
+    expert_out = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    E, cap, H = expert_out.shape
+    T, K = topk_idx.shape
+    y = np.empty((T, H), np.uint16)
+    status = _load().oracle_combine(_ptr(expert_out), E, cap, H, _ptr(topk_idx), _ptr(slot),
+                                    _ptr(topk_weights), T, K, _ptr(y))
+    return dict(y=y, status=status)
