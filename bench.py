@@ -1,0 +1,466 @@
+"""Benchmark: one step = layout -> FP8 dispatch -> combine over the 4096-token
+workload (H=7168, top-8 of 256 experts, 8 virtual ranks, cap = largest expert
+count), on one GB300 per process.
+
+Prints ONE JSON line.  `value` is the step's algorithmic HBM traffic (bytes
+read + written by layout, dispatch and combine) divided by the device-timed
+step, in GB/s, summed over ranks.  Per-kernel microseconds and GB/s, the
+roofline of the dominant kernel, an end-to-end number through the public API
+with host buffers, clocks, and the CPU oracle's speed on the same workload
+ride along.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: the
+path has no exchange step on one GPU, so ranks share no data.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "throughput"
+HBM_NOMINAL_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ----------------------------------------------------------------- bytes
+
+
+def algorithmic_bytes(T, H, K, E, R, cap, N, fp8):
+    """Bytes each kernel must move: every token row is read once (not K
+    times), unfilled capacity rows are not counted."""
+    G = H // 128
+    b = 1 if fp8 else 2
+    layout = 4 * T * K + 4 * T * K + T * R + 4 * E + 4 * R
+    dispatch = 2 * H * T + N * (H * b + (4 * G if fp8 else 0)) + 8 * T * K + 4 * E * cap
+    combine = N * 2 * H + 12 * T * K + 2 * T * H
+    return dict(layout=layout, dispatch=dispatch, combine=combine)
+
+
+def workload_config(c):
+    return {"workload": f"{c.name}: T={c.T} H={c.H} K={c.K} E={c.E} R={c.R} cap={c.cap} "
+                        "fp8 e4m3 dispatch (per-128 fp32 scales), bf16 combine, uniform routing",
+            "T": c.T, "H": c.H, "K": c.K, "E": c.E, "R": c.R, "cap": c.cap,
+            "dispatch_dtype": "e4m3", "combine_dtype": "bf16", "seed": c.seed}
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 10:
+                continue
+            try:
+                rows.append((ts, float(p[2]), float(p[3]), p[5], p[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[4]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ peaks
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        v = float(json.load(open(p))["hbm_gbs"])
+        return v, "measured (STREAM-style copy on this pool's GB300)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def ncu_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (matching source hash)."""
+    p = os.path.join(PROFILES, "ncu_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    if ent.get("source_sha256") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_full_launch")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_moedc_layout_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+def oracle_step(c, T_s: int):
+    """One oracle pass (layout, fp8 dispatch, combine) over the first T_s
+    tokens of the workload; returns (seconds, algorithmic bytes)."""
+    import oracle
+    from combine_moedc_layout_gb300 import synth
+
+    idx = np.ascontiguousarray(c.topk_idx[:T_s])
+    x = np.ascontiguousarray(c.x[:T_s])
+    w = np.ascontiguousarray(c.topk_weights[:T_s])
+    eo = c.extra["eo_host"]
+    t0 = time.perf_counter()
+    lay = oracle.layout(idx, c.E, c.R, c.cap)
+    oracle.dispatch(x, idx, lay["slot"], c.E, c.cap, fp8=c.dtype == synth.FP8_E4M3)
+    oracle.combine(eo, idx, lay["slot"], w)
+    dt = time.perf_counter() - t0
+    N = int(((idx >= 0) & (idx < c.E)).sum())
+    b = algorithmic_bytes(T_s, c.H, c.K, c.E, c.R, c.cap, N, c.dtype == synth.FP8_E4M3)
+    return dt, sum(b.values())
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def run_reference(args, rank: int) -> None:
+    if rank != 0:
+        return
+    from combine_moedc_layout_gb300 import synth
+    import oracle
+    oracle.build()
+    c = synth.make_case(WORKLOAD)
+    c.extra["eo_host"] = synth.make_expert_out(c, 0)
+    budget_s = 120.0
+    dt, _ = oracle_step(c, 32)                      # calibration, not timed
+    per_tok = dt / 32
+    T_s = int(max(1, min(c.T, budget_s / (args.steps + args.warmup) / per_tok)))
+    for _ in range(args.warmup):
+        oracle_step(c, T_s)
+    tot_t = 0.0
+    tot_b = 0
+    for _ in range(args.steps):
+        dt, b = oracle_step(c, T_s)
+        tot_t += dt
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    sample = (f"first {T_s} of {c.T} tokens of the workload per step (same H, K, E, R, cap); "
+              f"single-threaded plain-C oracle; {cpu_model()}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/bf16 (fp32 arithmetic)",
+            "data": "synthetic", "config": workload_config(c),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "dispatch & combine HBM GB/s (fraction of 8 TB/s) and us/call on 1 GB300"
+
+
+# ------------------------------------------------------------- GPU arm
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The slowest rank's time (every rank calls this)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
+    """Replicas each move step_bytes per step; the job's rate is bounded by
+    the slowest rank's step time."""
+    return step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+
+def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+
+    from combine_moedc_layout_gb300 import build as mbuild
+    from combine_moedc_layout_gb300 import moedc, synth
+
+    if rank == 0 or world == 1:
+        mbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    lib = moedc.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    c = synth.make_case(WORKLOAD)
+    fp8 = c.dtype == synth.FP8_E4M3
+    T, H, K, E, R, cap = c.T, c.H, c.K, c.E, c.R, c.cap
+    N = int(((c.topk_idx >= 0) & (c.topk_idx < E)).sum())
+    nbytes = algorithmic_bytes(T, H, K, E, R, cap, N, fp8)
+    step_bytes = sum(nbytes.values())
+
+    # inputs resident in HBM
+    x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(c.topk_idx).to(dev)
+    w = torch.from_numpy(c.topk_weights).to(dev)
+    eo_host = synth.make_expert_out(c, 0)
+    eo = torch.from_numpy(eo_host.view(np.int16)).view(torch.bfloat16).to(dev)
+    # outputs and scratch, caller-owned and reused every step
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    rk = torch.empty(R, dtype=torch.int32, device=dev)
+    inr = torch.empty((T, R), dtype=torch.uint8, device=dev)
+    sl = torch.empty((T, K), dtype=torch.int32, device=dev)
+    recv, scales, src = moedc.alloc_recv(E, cap, H, c.dtype, dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    wsb = moedc.moedc_layout_workspace_bytes(T, K, E, R)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    layout_kernels = 2 if wsb > 0 else 1
+    launches_per_step = layout_kernels + 2
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        r = moedc.moedc_layout(idx, T, K, E, R, cap, cnt, rk, inr, sl, ws, wsb, st, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        r |= moedc.moedc_dispatch(x, T, H, idx, sl, cnt, K, E, cap, c.dtype, recv, scales, src,
+                                  st, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        r |= moedc.moedc_combine(eo, E, cap, H, idx, sl, w, T, K, y, st, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        if r != 0:
+            raise RuntimeError(f"libmoedc returned {r}")
+
+    K_steps, W = args.steps, max(3, args.warmup)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.6)
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}: {moedc.strerror(int(st.item()))}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K_steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.3)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    total_ms = start.elapsed_time(end)
+    lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dis_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    com_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / K_steps
+    value = whole_job_gbs(step_bytes, world, ms_per_step)
+
+    def kstats(ms_list, b):
+        avg = sum(ms_list) / len(ms_list)
+        srt = sorted(ms_list)
+        return {"us_mean": avg * 1e3, "us_median": srt[len(srt) // 2] * 1e3,
+                "us_p10": srt[len(srt) // 10] * 1e3, "us_p90": srt[(9 * len(srt)) // 10] * 1e3,
+                "algorithmic_bytes": b, "gbs": b / (avg * 1e-3) / 1e9,
+                "frac_of_8tbs": b / (avg * 1e-3) / 1e9 / HBM_NOMINAL_GBS}
+
+    kern = {"layout": kstats(lay_ms, nbytes["layout"]),
+            "dispatch": kstats(dis_ms, nbytes["dispatch"]),
+            "combine": kstats(com_ms, nbytes["combine"])}
+    peak, peak_src = hbm_peak()
+    dom = max(("dispatch", "combine"), key=lambda k: kern[k]["us_mean"])
+    kname = {"dispatch": "dispatch_kernel", "combine": "combine_kernel"}[dom]
+    ach = kern[dom]["gbs"]
+    for k in ("dispatch", "combine"):
+        kern[k]["frac_of_measured_peak"] = kern[k]["gbs"] / peak
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "peak_source": peak_src + " (of measured)" if "measured" in
+                peak_src else peak_src, "traffic": ncu_traffic(kname),
+                "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = max(3, min(20, K_steps))
+    h_x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(c.topk_idx).pin_memory()
+    h_w = torch.from_numpy(c.topk_weights).pin_memory()
+    h_eo = torch.from_numpy(eo_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h_cnt = torch.empty(E, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_idx, h_w, h_eo))
+    d2h = h_y.numel() * 2 + h_cnt.numel() * 4
+
+    def e2e_step():
+        x.copy_(h_x, non_blocking=True)
+        idx.copy_(h_idx, non_blocking=True)
+        w.copy_(h_w, non_blocking=True)
+        eo.copy_(h_eo, non_blocking=True)
+        step()
+        h_y.copy_(y, non_blocking=True)
+        h_cnt.copy_(cnt, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_value = whole_job_gbs(step_bytes, world, e2e_ms)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        c.extra["eo_host"] = eo_host
+        dt, b = oracle_step(c, c.T)
+        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "seconds": dt,
+               "sample": f"one full step of the workload (all {c.T} tokens): layout, fp8 "
+                         f"dispatch, combine; single-threaded plain-C oracle; {cpu_model()}"}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": K_steps, "warmup": W, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 dispatch / bf16 combine (fp32 arithmetic)",
+            "data": "synthetic (seeded numpy: x~N(0,1) bf16, uniform distinct top-8)",
+            "config": dict(workload_config(c), parallelism=f"replicas x{world}",
+                           l2="inputs larger than L2: ~0.9 GB of HBM touched per step vs 129 MB "
+                              "L2, no flush"),
+            "frac_of_8tbs": value / world / HBM_NOMINAL_GBS,
+            "kernels": kern, "roofline": roofline,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
+                    "steps": e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "pinned host -> device copies of x, topk_idx, topk_weights, "
+                            "expert_out; moedc_layout, moedc_dispatch, moedc_combine; y and "
+                            "counts back to pinned host"},
+            "gpu_launches": launches_per_step * K_steps,
+            "clocks": clocks, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,39 @@
+// Entry points that launch nothing: version, status text, device query.
+#include "common.cuh"
+
+namespace moedc_host {
+
+int sm_count()
+{
+    // one cached value per device; reading it once per device keeps the
+    // attribute query off the per-call path
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace moedc_host
+
+extern "C" int moedc_api_version(void) { return MOEDC_API_VERSION; }
+
+extern "C" const char* moedc_strerror(int code)
+{
+    switch (code) {
+    case MOEDC_OK: return "ok";
+    case MOEDC_ERR_ARG: return "invalid argument (size, null or misaligned pointer, workspace)";
+    case MOEDC_ERR_CAPACITY: return "an expert received more entries than cap; extra entries dropped";
+    case MOEDC_ERR_EXPERT_RANGE: return "a top-k index lies outside [-1, E); entry treated as masked";
+    case MOEDC_ERR_CUDA: return "a CUDA launch failed";
+    case MOEDC_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case MOEDC_ERR_UNIMPLEMENTED: return "not implemented";
+    default: return "unknown status code";
+    }
+}

@@ -1,0 +1,98 @@
+// Shared device helpers for the libmoedc kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moedc.h"
+
+namespace moedc {
+
+constexpr int kWarp = 32;
+
+// Raise the caller's status word to max(*status, code): the result does not
+// depend on which thread reports first.
+__device__ __forceinline__ void raise_status(int32_t* status, int code)
+{
+    atomicMax(status, code);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt()
+{
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// bf16 bit pattern -> binary32 (exact widening).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// binary32 -> bf16, round to nearest even (hardware cvt.rn.bf16x2.f32);
+// `lo` lands in the low half of the result.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two binary32 values -> two e4m3fn codes, round to nearest even with
+// saturation to +-448 (cvt.rn.satfinite.e4m3x2.f32); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
+{
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Plain 16-byte global accesses.  Streaming stores: written rows are not
+// re-read by this kernel, so they should not displace reusable lines.
+__device__ __forceinline__ uint4 ld_global_nc(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global_cs(uint4* p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_global_cs_f32(float* p, float v)
+{
+    asm volatile("st.global.cs.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+}
+
+}  // namespace moedc
+
+// Host-side helpers shared by the entry points.
+namespace moedc_host {
+
+int sm_count();                 // multiprocessors of the current device
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int launch_status() { return cudaGetLastError() == cudaSuccess ? MOEDC_OK : MOEDC_ERR_CUDA; }
+
+// Layout geometry: tokens per thread block of the layout kernels.
+struct LayoutGeom {
+    int tpc;        // tokens per block
+    int blocks;     // number of blocks (>= 1)
+    size_t ws;      // workspace bytes (0 when blocks == 1)
+};
+LayoutGeom layout_geometry(int T, int K, int E, int R);
+bool layout_args_ok(int T, int K, int E, int R, int cap);
+
+// Launches of the layout kernels (layout.cu); used by the fused entry point.
+int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
+                  int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                  uint8_t* is_token_in_rank, int32_t* slot, void* workspace,
+                  int32_t* dev_status, cudaStream_t stream);
+int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const int32_t* slot,
+                    const int32_t* num_tokens_per_expert, int K, int E, int cap, int out_dtype,
+                    void* recv, float* scales, int32_t* src_idx, int32_t* dev_status,
+                    cudaStream_t stream);
+
+}  // namespace moedc_host

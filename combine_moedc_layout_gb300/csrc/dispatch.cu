@@ -1,0 +1,126 @@
+// Dispatch: scatter token rows into expert slots (bf16 copy or e4m3 + scales)
+// and write the per-slot source-token index.
+//
+// Sources: DeepEP PR #693 "Pipeline direct NVLink dispatch with
+// triple-buffered prefetch", Summary (hidden data, scale factors and routing
+// of a token move together); MORI PR #614 "perf(ep): InterNodeV1LL low-token
+// latency on MI300X + CX7" (flat stride over work items instead of per-block
+// token ranges).  On one GPU the "remote store" is a plain HBM store, so the
+// kernel is a write stream: each token row is read once and written K times.
+#include "dispatch_item.cuh"
+
+namespace moedc {
+
+constexpr int kDispatchThreads = 256;
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
+                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
+                const int32_t* __restrict__ num_tokens_per_expert, int K, int E, int cap,
+                void* __restrict__ recv, float* __restrict__ scales,
+                int32_t* __restrict__ src_idx, int32_t* __restrict__ status)
+{
+    const int lane = threadIdx.x % kWarp;
+    const int nslice = (H + kSlice - 1) / kSlice;
+    const int64_t items = (int64_t)T * nslice;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    bool bad = false;
+
+    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+         item < items; item += nwarps) {
+        const int t = (int)(item / nslice);
+        const int sl = (int)(item - (int64_t)t * nslice);
+        int my_e = -1, my_s = -1;
+        if (lane < K) {
+            my_e = topk_idx[(int64_t)t * K + lane];
+            my_s = slot[(int64_t)t * K + lane];
+        }
+        if (sl == 0 && lane < K) {
+            if (my_e < -1 || my_e >= E) bad = true;
+            if (dest_ok(my_e, my_s, E, cap)) src_idx[(int64_t)my_e * cap + my_s] = t;
+        }
+        const uint16_t* xrow = x + (int64_t)t * H;
+        if (kFp8)
+            dispatch_slice_fp8(xrow, H, sl, lane, K, my_e, my_s, E, cap,
+                               static_cast<uint8_t*>(recv), scales);
+        else
+            dispatch_slice_bf16(xrow, H, sl, lane, K, my_e, my_s, E, cap,
+                                static_cast<uint16_t*>(recv));
+    }
+    if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+
+    // slots no entry reaches carry src_idx = -1
+    const int64_t total = (int64_t)E * cap;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += nthreads) {
+        const int e = (int)(i / cap);
+        const int s = (int)(i - (int64_t)e * cap);
+        if (s >= __ldg(num_tokens_per_expert + e)) src_idx[i] = -1;
+    }
+}
+
+}  // namespace moedc
+
+namespace moedc_host {
+
+static bool dispatch_args_ok(const void* x, int T, int H, const int32_t* topk_idx,
+                             const int32_t* slot, const int32_t* cnt, int K, int E, int cap,
+                             int out_dtype, const void* recv, const float* scales,
+                             const int32_t* src_idx, const int32_t* dev_status)
+{
+    if (T < 0 || H < 8 || K < 1 || K > MOEDC_MAX_K || E < 1 || E > MOEDC_MAX_E || cap < 1)
+        return false;
+    if (out_dtype != MOEDC_BF16 && out_dtype != MOEDC_FP8_E4M3) return false;
+    if (out_dtype == MOEDC_BF16 && H % 8 != 0) return false;
+    if (out_dtype == MOEDC_FP8_E4M3 && H % 128 != 0) return false;
+    if (!cnt || !recv || !src_idx || !dev_status) return false;
+    if (out_dtype == MOEDC_FP8_E4M3 && !scales) return false;
+    if (T > 0 && (!x || !topk_idx || !slot)) return false;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(scales, 4) || !aligned(topk_idx, 4) ||
+        !aligned(slot, 4) || !aligned(cnt, 4) || !aligned(src_idx, 4) || !aligned(dev_status, 4))
+        return false;
+    return true;
+}
+
+int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const int32_t* slot,
+                    const int32_t* num_tokens_per_expert, int K, int E, int cap, int out_dtype,
+                    void* recv, float* scales, int32_t* src_idx, int32_t* dev_status,
+                    cudaStream_t stream)
+{
+    const int warps_per_block = moedc::kDispatchThreads / moedc::kWarp;
+    const int nslice = (H + moedc::kSlice - 1) / moedc::kSlice;
+    const int64_t items = (int64_t)T * nslice;
+    const int64_t fill = (int64_t)E * cap;
+    int64_t blocks = (items + warps_per_block - 1) / warps_per_block;
+    const int64_t fill_blocks = (fill + moedc::kDispatchThreads - 1) / moedc::kDispatchThreads;
+    if (blocks < fill_blocks) blocks = fill_blocks;
+    const int64_t max_blocks = (int64_t)sm_count() * 8;   // 8 x 256 threads fill an SM
+    if (blocks > max_blocks) blocks = max_blocks;
+    if (blocks < 1) blocks = 1;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (out_dtype == MOEDC_FP8_E4M3)
+        moedc::dispatch_kernel<true><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
+            xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
+            dev_status);
+    else
+        moedc::dispatch_kernel<false><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
+            xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
+            dev_status);
+    return launch_status();
+}
+
+}  // namespace moedc_host
+
+extern "C" int moedc_dispatch(const void* x, int T, int H, const int32_t* topk_idx,
+                              const int32_t* slot, const int32_t* num_tokens_per_expert, int K,
+                              int E, int cap, int out_dtype, void* recv, float* scales,
+                              int32_t* src_idx, int32_t* dev_status, cudaStream_t stream)
+{
+    using namespace moedc_host;
+    if (!dispatch_args_ok(x, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, out_dtype,
+                          recv, scales, src_idx, dev_status))
+        return MOEDC_ERR_ARG;
+    return launch_dispatch(x, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, out_dtype,
+                           recv, scales, src_idx, dev_status, stream);
+}

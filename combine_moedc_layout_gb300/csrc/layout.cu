@@ -1,0 +1,302 @@
+// Routing layout: per-expert histogram, per-rank distinct-token counts,
+// token-in-rank mask and the deterministic per-expert slot map.
+//
+// Sources: UCCL PR #749 "[EP] Low-latency mode batch tokens per destination"
+// (code excerpt: the per-expert routed-token counter and the per-destination
+// rank total built from the rank's local experts; its note that the send
+// waits on the counts of all of a rank's experts is why the layout here is a
+// complete pass that finishes before dispatch starts), and MORI PR #614
+// "perf(ep): InterNodeV1LL low-token latency on MI300X + CX7" (routing-scan
+// note: the topk loads are issued together and a negative sentinel expert is
+// tested before any division).
+//
+// Two kernels, no atomics that decide order:
+//   count  (skipped when one block holds every token): block c histograms its
+//          contiguous run of tokens into workspace row c, and counts the
+//          distinct tokens it sends to each rank.
+//   assign: block c turns the rows of blocks < c into per-expert base offsets,
+//          splits its own run over 8 warps (per-warp counts + a scan across
+//          warps), then each warp walks its entries in order and ranks equal
+//          experts inside a 32-entry tile with __match_any_sync.  The last
+//          block also writes the totals.
+#include "common.cuh"
+
+namespace moedc {
+
+constexpr int kLayoutThreads = 256;
+constexpr int kLayoutWarps = kLayoutThreads / kWarp;
+constexpr int kEntriesPerBlock = 1024;     // target (token, k) entries per block
+constexpr int kSingleBlockEntries = 2048;  // up to here one block does everything
+constexpr int kMaxLayoutBlocks = 1024;
+
+__device__ __forceinline__ bool valid_expert(int e, int E) { return e >= 0 && e < E; }
+
+// does token row `row` (K entries in shared memory) send anything to rank r?
+__device__ __forceinline__ bool token_in_rank(const int32_t* row, int K, int E, int epr, int r)
+{
+    for (int k = 0; k < K; ++k) {
+        int e = row[k];
+        if (valid_expert(e, E) && e / epr == r)
+            return true;
+    }
+    return false;
+}
+
+// is entry k the first of its token row that goes to rank r?
+__device__ __forceinline__ bool first_in_rank(const int32_t* row, int k, int E, int epr, int r)
+{
+    for (int j = 0; j < k; ++j) {
+        int e = row[j];
+        if (valid_expert(e, E) && e / epr == r)
+            return false;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_count_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, int R, int tpc,
+                    int32_t* __restrict__ ws_hist, int32_t* __restrict__ ws_rank,
+                    int32_t* __restrict__ status)
+{
+    extern __shared__ int32_t smem[];
+    int32_t* s_idx = smem;                // [tpc * K]
+    int32_t* s_hist = s_idx + tpc * K;    // [E]
+    int32_t* s_rank = s_hist + E;         // [R]
+
+    const int c = blockIdx.x;
+    const int t0 = c * tpc;
+    const int nt = min(tpc, T - t0);
+    const int n = nt * K;
+    const int epr = E / R;
+
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
+    for (int i = threadIdx.x; i < R; i += blockDim.x) s_rank[i] = 0;
+    const int32_t* src = topk_idx + (int64_t)t0 * K;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = src[i];
+    __syncthreads();
+
+    bool bad = false;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int e = s_idx[i];
+        if (e == -1) continue;
+        if (!valid_expert(e, E)) { bad = true; continue; }
+        atomicAdd(&s_hist[e], 1);
+        const int k = i % K;
+        const int r = e / epr;
+        if (first_in_rank(s_idx + (i - k), k, E, epr, r))
+            atomicAdd(&s_rank[r], 1);
+    }
+    if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) ws_hist[(int64_t)c * E + i] = s_hist[i];
+    for (int i = threadIdx.x; i < R; i += blockDim.x) ws_rank[(int64_t)c * R + i] = s_rank[i];
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_assign_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, int R, int cap,
+                     int tpc, const int32_t* __restrict__ ws_hist,
+                     const int32_t* __restrict__ ws_rank,
+                     int32_t* __restrict__ num_tokens_per_expert,
+                     int32_t* __restrict__ num_tokens_per_rank,
+                     uint8_t* __restrict__ is_token_in_rank, int32_t* __restrict__ slot,
+                     int32_t* __restrict__ status)
+{
+    extern __shared__ int32_t smem[];
+    int32_t* s_idx = smem;                          // [tpc * K]
+    int32_t* s_whist = s_idx + tpc * K;             // [kLayoutWarps][E]
+    int32_t* s_base = s_whist + kLayoutWarps * E;   // [E]
+    int32_t* s_rank = s_base + E;                   // [R]
+
+    const int c = blockIdx.x;
+    const bool last = (c == gridDim.x - 1);
+    const int t0 = c * tpc;
+    const int nt = max(0, min(tpc, T - t0));
+    const int n = nt * K;
+    const int epr = E / R;
+    const int warp = threadIdx.x / kWarp;
+    const int lane = threadIdx.x % kWarp;
+
+    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s_whist[i] = 0;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s_base[i] = 0;
+    for (int i = threadIdx.x; i < R; i += blockDim.x) s_rank[i] = 0;
+    const int32_t* src = topk_idx + (int64_t)t0 * K;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = src[i];
+    __syncthreads();
+
+    // base offsets: entries routed to each expert by the blocks before this one
+    {
+        const int m = c * E;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < m; i += blockDim.x)
+            atomicAdd(&s_base[i % E], ws_hist[i]);
+    }
+    if (last) {
+        const int m = c * R;
+        for (int i = threadIdx.x; i < m; i += blockDim.x)
+            atomicAdd(&s_rank[i % R], ws_rank[i]);
+        bool bad = false;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int e = s_idx[i];
+            if (e == -1) continue;
+            if (!valid_expert(e, E)) { bad = true; continue; }
+            const int k = i % K;
+            const int r = e / epr;
+            if (first_in_rank(s_idx + (i - k), k, E, epr, r))
+                atomicAdd(&s_rank[r], 1);
+        }
+        if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+    }
+
+    // each warp owns a contiguous run of whole 32-entry tiles
+    const int run = ((n + kLayoutWarps * kWarp - 1) / (kLayoutWarps * kWarp)) * kWarp;
+    const int wbeg = min(n, warp * run);
+    const int wend = min(n, wbeg + run);
+    int32_t* my_hist = s_whist + warp * E;
+    for (int i = wbeg + lane; i < wend; i += kWarp) {
+        const int e = s_idx[i];
+        if (valid_expert(e, E)) atomicAdd(&my_hist[e], 1);
+    }
+    __syncthreads();
+
+    // exclusive scan across warps, on top of the block's base offset
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int acc = s_base[e];
+#pragma unroll
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int v = s_whist[w * E + e];
+            s_whist[w * E + e] = acc;
+            acc += v;
+        }
+        if (last) {
+            num_tokens_per_expert[e] = acc;
+            if (acc > cap) raise_status(status, MOEDC_ERR_CAPACITY);
+        }
+    }
+    if (last)
+        for (int r = threadIdx.x; r < R; r += blockDim.x) num_tokens_per_rank[r] = s_rank[r];
+    __syncthreads();
+
+    // slots, tile by tile in entry order
+    const unsigned lt = lanemask_lt();
+    int32_t* dst = slot + (int64_t)t0 * K;
+    for (int i0 = wbeg; i0 < wend; i0 += kWarp) {
+        const int i = i0 + lane;
+        const int e = (i < wend) ? s_idx[i] : -1;
+        const bool v = valid_expert(e, E);
+        const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1);
+        int s = -1;
+        if (v) s = my_hist[e] + __popc(peers & lt);
+        __syncwarp();
+        if (v && (peers & lt) == 0) my_hist[e] += __popc(peers);
+        __syncwarp();
+        if (i < wend) dst[i] = s;
+    }
+
+    // token-in-rank rows of this block's tokens
+    uint8_t* rows = is_token_in_rank + (int64_t)t0 * R;
+    for (int b = threadIdx.x; b < nt * R; b += blockDim.x) {
+        const int t = b / R;
+        const int r = b - t * R;
+        rows[b] = token_in_rank(s_idx + t * K, K, E, epr, r) ? 1 : 0;
+    }
+}
+
+size_t count_smem(int tpc, int K, int E, int R) { return (size_t)(tpc * K + E + R) * 4; }
+size_t assign_smem(int tpc, int K, int E, int R)
+{
+    return (size_t)(tpc * K + kLayoutWarps * E + E + R) * 4;
+}
+
+}  // namespace moedc
+
+namespace moedc_host {
+
+bool layout_args_ok(int T, int K, int E, int R, int cap)
+{
+    if (T < 0 || K < 1 || K > MOEDC_MAX_K || E < 1 || E > MOEDC_MAX_E || R < 1 || R > E ||
+        E % R != 0 || cap < 1)
+        return false;
+    if ((int64_t)T * K > (int64_t)moedc::kMaxLayoutBlocks * 16384)
+        return false;
+    return true;
+}
+
+LayoutGeom layout_geometry(int T, int K, int E, int R)
+{
+    LayoutGeom g{};
+    const int64_t n = (int64_t)T * K;
+    if (n <= moedc::kSingleBlockEntries) {
+        g.tpc = T;
+        g.blocks = 1;
+        g.ws = 0;
+        return g;
+    }
+    int tpc = (moedc::kEntriesPerBlock + K - 1) / K;
+    const int min_tpc = (T + moedc::kMaxLayoutBlocks - 1) / moedc::kMaxLayoutBlocks;
+    if (tpc < min_tpc) tpc = min_tpc;
+    g.tpc = tpc;
+    g.blocks = (T + tpc - 1) / tpc;
+    g.ws = (size_t)g.blocks * (size_t)(E + R) * sizeof(int32_t);
+    return g;
+}
+
+static int ensure_smem_attr(const void* fn, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return MOEDC_OK;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+                   cudaSuccess
+               ? MOEDC_OK
+               : MOEDC_ERR_CUDA;
+}
+
+int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
+                  int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                  uint8_t* is_token_in_rank, int32_t* slot, void* workspace,
+                  int32_t* dev_status, cudaStream_t stream)
+{
+    const LayoutGeom g = layout_geometry(T, K, E, R);
+    int32_t* ws_hist = static_cast<int32_t*>(workspace);
+    int32_t* ws_rank = ws_hist ? ws_hist + (size_t)g.blocks * E : nullptr;
+    if (g.blocks > 1) {
+        const size_t sm = moedc::count_smem(g.tpc, K, E, R);
+        if (ensure_smem_attr((const void*)moedc::layout_count_kernel, sm) != MOEDC_OK)
+            return MOEDC_ERR_CUDA;
+        moedc::layout_count_kernel<<<g.blocks, moedc::kLayoutThreads, sm, stream>>>(
+            topk_idx, T, K, E, R, g.tpc, ws_hist, ws_rank, dev_status);
+        if (launch_status() != MOEDC_OK) return MOEDC_ERR_CUDA;
+    }
+    const size_t sm = moedc::assign_smem(g.tpc, K, E, R);
+    if (ensure_smem_attr((const void*)moedc::layout_assign_kernel, sm) != MOEDC_OK)
+        return MOEDC_ERR_CUDA;
+    moedc::layout_assign_kernel<<<g.blocks, moedc::kLayoutThreads, sm, stream>>>(
+        topk_idx, T, K, E, R, cap, g.tpc, ws_hist, ws_rank, num_tokens_per_expert,
+        num_tokens_per_rank, is_token_in_rank, slot, dev_status);
+    return launch_status();
+}
+
+}  // namespace moedc_host
+
+extern "C" size_t moedc_layout_workspace_bytes(int T, int K, int E, int R)
+{
+    if (!moedc_host::layout_args_ok(T, K, E, R, 1)) return 0;
+    return moedc_host::layout_geometry(T, K, E, R).ws;
+}
+
+extern "C" int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
+                            int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                            uint8_t* is_token_in_rank, int32_t* slot, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream)
+{
+    using namespace moedc_host;
+    if (!layout_args_ok(T, K, E, R, cap)) return MOEDC_ERR_ARG;
+    if (!num_tokens_per_expert || !num_tokens_per_rank || !dev_status) return MOEDC_ERR_ARG;
+    if (T > 0 && (!topk_idx || !is_token_in_rank || !slot)) return MOEDC_ERR_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(slot, 4) || !aligned(num_tokens_per_expert, 4) ||
+        !aligned(num_tokens_per_rank, 4) || !aligned(dev_status, 4))
+        return MOEDC_ERR_ARG;
+    const LayoutGeom g = layout_geometry(T, K, E, R);
+    if (g.ws > 0 && (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)))
+        return MOEDC_ERR_ARG;
+    return launch_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,
+                         is_token_in_rank, slot, workspace, dev_status, stream);
+}

@@ -1,0 +1,194 @@
+/*
+ * libmoedc — MoE expert-parallel token layout, dispatch and combine on one
+ * GPU, with R "virtual ranks" that partition the expert dimension of a single
+ * receive buffer (no inter-GPU transport).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  T tokens, H hidden channels, K routed experts per token, E experts,
+ *  R virtual ranks (rank r owns experts [r*E/R, (r+1)*E/R); E % R == 0),
+ *  cap slots per expert, G = H / 128 FP8 scale groups.
+ *
+ *  Every pointer is a DEVICE pointer owned by the caller.  The library never
+ *  allocates, frees or synchronises, keeps no state between calls and reads
+ *  no environment variable.  Calls are asynchronous on `stream` (0 = the
+ *  legacy default stream) and contain no host-side reads of device data.
+ *
+ *  Row-major layouts:
+ *    x, y                 bf16   [T, H]
+ *    topk_idx             int32  [T, K]   -1 = masked entry
+ *    topk_weights         fp32   [T, K]
+ *    slot                 int32  [T, K]   -1 = masked / dropped
+ *    num_tokens_per_expert int32 [E]
+ *    num_tokens_per_rank  int32  [R]
+ *    is_token_in_rank     uint8  [T, R]   0 / 1
+ *    recv, expert_out     bf16 or e4m3 [E, cap, H]   (expert-major)
+ *    scales               fp32   [E, cap, G]
+ *    src_idx              int32  [E, cap]
+ *  x, y, recv and expert_out must be 16-byte aligned; the others 4-byte
+ *  aligned (is_token_in_rank: any alignment).
+ *
+ * Errors
+ * ------
+ *  The return value reports argument errors found on the host (bad sizes,
+ *  null or misaligned pointers, a workspace that is too small); nothing is
+ *  launched when it is not MOEDC_OK.  MOEDC_ERR_CUDA means a launch failed.
+ *  Errors that depend on the data are written to `dev_status`, a device int32
+ *  the caller zeroes: each kernel raises it to max(*dev_status, code), so the
+ *  word ends up holding the largest code met, independent of thread timing.
+ *  A clean run leaves it untouched.
+ *    MOEDC_ERR_EXPERT_RANGE  an index outside [-1, E); the entry is treated
+ *                            as masked.
+ *    MOEDC_ERR_CAPACITY      an expert received more than cap entries; the
+ *                            slots still count on, and the entries whose slot
+ *                            is >= cap are dropped by dispatch and combine.
+ *
+ * Sources (page title, part of the page):
+ *  [UCCL749]  UCCL PR #749 "[EP] Low-latency mode batch tokens per
+ *             destination", code excerpt (per-expert routed-token counters,
+ *             per-destination-rank token totals over the rank's experts).
+ *  [DEEPEP693] DeepEP PR #693 "Pipeline direct NVLink dispatch with
+ *             triple-buffered prefetch", Summary (token rows staged through
+ *             shared memory; hidden data, scale factors and routing move
+ *             together).
+ *  [MORI614]  MORI PR #614 "perf(ep): InterNodeV1LL low-token latency on
+ *             MI300X + CX7": the notes on DispatchIntraNode's flat stride,
+ *             CombineSync's (token, hidden slice) split, the MultiWarpIter
+ *             512-element floor, block-local relay without grid barriers,
+ *             the zero-copy combine input, the host view cache, and the
+ *             negative sentinel expert.
+ */
+#ifndef MOEDC_H
+#define MOEDC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOEDC_API_VERSION 1
+
+#if defined(__GNUC__)
+#define MOEDC_EXPORT __attribute__((visibility("default")))
+#else
+#define MOEDC_EXPORT
+#endif
+
+typedef enum {
+    MOEDC_OK = 0,
+    MOEDC_ERR_ARG = 1,
+    MOEDC_ERR_CAPACITY = 2,
+    MOEDC_ERR_EXPERT_RANGE = 3,
+    MOEDC_ERR_CUDA = 4,
+    MOEDC_ERR_TIMEOUT = 5,
+    MOEDC_ERR_UNIMPLEMENTED = 6
+} moedc_status;
+
+typedef enum { MOEDC_BF16 = 0, MOEDC_FP8_E4M3 = 1 } moedc_dtype;
+
+/* Limits checked on the host (MOEDC_ERR_ARG beyond them). */
+#define MOEDC_MAX_K 32
+#define MOEDC_MAX_E 1024
+
+/* Version of this interface (MOEDC_API_VERSION of the build). */
+MOEDC_EXPORT int moedc_api_version(void);
+
+/* Static text for a status code; never NULL. */
+MOEDC_EXPORT const char* moedc_strerror(int code);
+
+/*
+ * Bytes of device scratch that moedc_layout / moedc_layout_dispatch need for
+ * this shape (0 when the whole layout fits one thread block).  The caller
+ * allocates it (any 16-byte aligned device buffer of at least this size) and
+ * may reuse it across calls that are ordered on one stream.  Returns 0 for
+ * arguments that the layout would reject.
+ */
+MOEDC_EXPORT size_t moedc_layout_workspace_bytes(int T, int K, int E, int R);
+
+/*
+ * Routing layout [UCCL749 code excerpt; MORI614 sentinel note].
+ * Visiting entries (t, k) in ascending t, then k:
+ *   slot[t][k]              = number of earlier entries routed to the same
+ *                             expert (so each expert's slots run 0, 1, ... in
+ *                             ascending source-token order); -1 if masked.
+ *   num_tokens_per_expert[e] = entries routed to expert e.
+ *   is_token_in_rank[t][r]  = 1 if any entry of token t goes to rank r.
+ *   num_tokens_per_rank[r]  = number of distinct tokens with a 1 in column r.
+ * Arguments: T >= 0, 1 <= K <= MOEDC_MAX_K, 1 <= E <= MOEDC_MAX_E,
+ * 1 <= R <= E with E % R == 0, cap >= 1.  workspace may be NULL only when
+ * moedc_layout_workspace_bytes() returns 0.
+ * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE, MOEDC_ERR_CAPACITY.
+ */
+MOEDC_EXPORT int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
+                 int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                 uint8_t* is_token_in_rank, int32_t* slot,
+                 void* workspace, size_t workspace_bytes,
+                 int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Dispatch [DEEPEP693 Summary; MORI614 DispatchIntraNode note].
+ * For every entry (t, k) with expert e in [0, E) and slot s in [0, cap):
+ *   src_idx[e][s] = t
+ *   MOEDC_BF16:     recv[e][s][:] = x[t][:]  (bit copy; recv is bf16)
+ *   MOEDC_FP8_E4M3: per group g of 128 channels, a = max |x[t][128g+i]|,
+ *                   a = max(a, 1e-4f), sc = a / 448 (IEEE binary32 division),
+ *                   recv[e][s][128g+i] = e4m3fn(x / sc) with one binary32
+ *                   division and round-to-nearest-even, saturating to +-448;
+ *                   scales[e][s][g] = sc.
+ * src_idx[e][s] = -1 for every s in [num_tokens_per_expert[e], cap).
+ * Rows of recv / scales that no entry reaches are not written.
+ * num_tokens_per_expert and slot are the outputs of moedc_layout for the same
+ * topk_idx.  Arguments: T >= 0, H >= 8 with H % 8 == 0 (bf16) or
+ * H % 128 == 0 (e4m3), K, E and cap as for moedc_layout; scales may be NULL
+ * for MOEDC_BF16.
+ * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE.
+ */
+MOEDC_EXPORT int moedc_dispatch(const void* x, int T, int H,
+                   const int32_t* topk_idx, const int32_t* slot,
+                   const int32_t* num_tokens_per_expert,
+                   int K, int E, int cap, int out_dtype,
+                   void* recv, float* scales, int32_t* src_idx,
+                   int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Combine [MORI614 CombineSync and zero-copy combine input notes].
+ *   y[t][h] = bf16_rne( sum over k = 0..K-1 ascending of
+ *                       w[t][k] * float(expert_out[e][s][h]) )
+ * with a binary32 accumulator that starts at +0, one rounded multiply and one
+ * rounded add per term (never fused), skipping entries that are masked,
+ * out of range, or have slot >= cap.  expert_out is read in place (bf16).
+ * Arguments: T >= 0, H % 8 == 0, K, E and cap as for moedc_layout.
+ * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE.
+ */
+MOEDC_EXPORT int moedc_combine(const void* expert_out, int E, int cap, int H,
+                  const int32_t* topk_idx, const int32_t* slot,
+                  const float* topk_weights, int T, int K,
+                  void* y, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Layout followed by dispatch, with the outputs of both calls
+ * [MORI614 notes on low token counts: host enqueue and idle warps dominate].
+ * For T * K <= MOEDC_FUSED_MAX_ENTRIES this is ONE kernel launch: every
+ * thread block rebuilds the layout in shared memory (no inter-block
+ * synchronisation), block 0 writes the layout outputs, and all blocks split
+ * the (token, 512-channel slice) copies.  Larger inputs run moedc_layout and
+ * moedc_dispatch back to back.  Results are identical either way.
+ * workspace: as for moedc_layout (never used on the single-launch path).
+ */
+#define MOEDC_FUSED_MAX_ENTRIES 1024
+MOEDC_EXPORT int moedc_layout_dispatch(const void* x, const int32_t* topk_idx,
+                          int T, int H, int K, int E, int R, int cap, int out_dtype,
+                          int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                          uint8_t* is_token_in_rank, int32_t* slot,
+                          void* recv, float* scales, int32_t* src_idx,
+                          void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEDC_H */

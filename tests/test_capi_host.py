@@ -1,0 +1,135 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every entry point the header declares, and rejects bad
+arguments before touching CUDA.  Also the benchmark's byte accounting and
+its multi-rank reduction (gloo, two processes)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from combine_moedc_layout_gb300 import build as mbuild
+from combine_moedc_layout_gb300 import moedc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return moedc.load()
+
+
+def declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"MOEDC_EXPORT\s+[\w\s\*]+?\b(moedc_\w+)\s*\(", src))
+    return names
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_symbols()
+    assert {"moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
+            "moedc_strerror", "moedc_api_version", "moedc_layout_workspace_bytes"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", mbuild.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(moedc_\w+)", out))
+    missing = declared_symbols() - exported
+    assert not missing, missing
+    for name in declared_symbols():
+        assert hasattr(lib, name)
+    # nothing but the declared C entry points is visible
+    assert exported == declared_symbols()
+
+
+def test_version_and_strerror(lib):
+    assert lib.moedc_api_version() == 1
+    for code in range(7):
+        assert moedc.strerror(code) and "unknown" not in moedc.strerror(code)
+    assert "unknown" in moedc.strerror(99)
+
+
+def test_workspace_bytes(lib):
+    # one block handles up to 2048 entries: no scratch
+    assert moedc.moedc_layout_workspace_bytes(64, 4, 32, 4) == 0
+    assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == 0
+    # 4096 x 8 entries: 128 tokens per block -> 32 blocks x (E + R) int32
+    assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 32 * (256 + 8) * 4
+    # rejected shapes report 0
+    assert moedc.moedc_layout_workspace_bytes(4096, 8, 250, 8) == 0
+    assert moedc.moedc_layout_workspace_bytes(4096, 0, 256, 8) == 0
+
+
+def test_argument_errors_return_before_cuda(lib):
+    P = ctypes.c_void_p
+    fake = P(256)             # never dereferenced: validation fails first
+    # K = 0, E % R != 0, E too large, cap = 0
+    for (T, K, E, R, cap) in [(4, 0, 8, 2, 4), (4, 2, 9, 2, 4), (4, 2, 2048, 2, 4),
+                              (4, 2, 8, 2, 0), (-1, 2, 8, 2, 4), (4, 33, 64, 2, 4)]:
+        assert lib.moedc_layout(fake, T, K, E, R, cap, fake, fake, fake, fake, None, 0, fake,
+                                None) == moedc.ERR_ARG
+    # dispatch: fp8 with H % 128 != 0; bad dtype; null scales for fp8
+    assert lib.moedc_dispatch(fake, 4, 200, fake, fake, fake, 2, 8, 4, moedc.FP8_E4M3, fake,
+                              fake, fake, fake, None) == moedc.ERR_ARG
+    assert lib.moedc_dispatch(fake, 4, 256, fake, fake, fake, 2, 8, 4, 7, fake, fake, fake,
+                              fake, None) == moedc.ERR_ARG
+    assert lib.moedc_dispatch(fake, 4, 256, fake, fake, fake, 2, 8, 4, moedc.FP8_E4M3, fake,
+                              None, fake, fake, None) == moedc.ERR_ARG
+    # misaligned x (bf16 needs 16-byte alignment)
+    assert lib.moedc_dispatch(P(258), 4, 256, fake, fake, fake, 2, 8, 4, moedc.BF16, fake,
+                              None, fake, fake, None) == moedc.ERR_ARG
+    # combine: H % 8 != 0, null y
+    assert lib.moedc_combine(fake, 8, 4, 100, fake, fake, fake, 4, 2, fake, fake, None) == \
+        moedc.ERR_ARG
+    assert lib.moedc_combine(fake, 8, 4, 128, fake, fake, fake, 4, 2, None, fake, None) == \
+        moedc.ERR_ARG
+    # fused: multi-block shape without workspace
+    assert lib.moedc_layout_dispatch(fake, fake, 4096, 256, 8, 64, 8, 600, moedc.BF16, fake,
+                                     fake, fake, fake, fake, None, fake, None, 0, fake,
+                                     None) == moedc.ERR_ARG
+
+
+def test_bench_byte_accounting():
+    import bench
+    b = bench.algorithmic_bytes(T=4096, H=7168, K=8, E=256, R=8, cap=160, N=32768, fp8=True)
+    # read x once per token + 32768 e4m3 rows with 56 fp32 scales + idx/slot + src_idx
+    assert b["dispatch"] == 2 * 7168 * 4096 + 32768 * (7168 + 224) + 8 * 4096 * 8 + 4 * 256 * 160
+    assert abs(b["dispatch"] / 1e6 - 301.4) < 0.1
+    assert abs(b["combine"] / 1e6 - 528.9) < 0.1
+    assert bench.whole_job_gbs(10**9, 2, 1.0) == pytest.approx(2000.0)
+
+
+def _gloo_worker(rank, world, port, q):
+    import torch.distributed as dist
+
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    slowest = bench.max_over_ranks(1.0 + rank, world)
+    q.put((rank, slowest, bench.whole_job_gbs(10**9, world, slowest)))
+    dist.destroy_process_group()
+
+
+def test_bench_max_over_ranks_gloo_two_processes():
+    import multiprocessing as mp
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    ps = [ctx.Process(target=_gloo_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(timeout=120)
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert [r[1] for r in res] == [2.0, 2.0]            # both see the slowest rank
+    assert all(abs(r[2] - 1000.0) < 1e-9 for r in res)  # 2 x 1 GB / 2 ms

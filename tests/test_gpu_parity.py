@@ -1,0 +1,286 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle,
+element by element on the same seeded bytes.
+
+Bar: layout, src_idx, recv rows (bf16 bits or e4m3 codes) and fp32 scales
+are bit-exact; combine is within 1 bf16 ulp of |y| and, by construction,
+bit-exact too.  Full-size workloads run in the same launch configuration the
+benchmark uses (the library picks its own geometry from the shapes).
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moedc_layout_gb300 import moedc, synth
+from parity_util import (DevCase, bits_host, compare_combine, compare_dispatch, compare_layout,
+                         expert_out_dev, run_layout)
+
+pytestmark = pytest.mark.gpu
+
+NAMED = ["tiny", "low4", "low8", "low16", "default_ll", "throughput", "imbalanced"]
+
+
+@functools.lru_cache(maxsize=None)
+def named(name):
+    return synth.make_case(name)
+
+
+RANDOM = {
+    # multi-block layout, ragged tail of tokens and of 512-channel slices
+    "multiblock_bf16": dict(seed=11, T=3001, H=1160, K=6, E=96, R=12, cap=None, dtype=synth.BF16,
+                            mask_p=0.07),
+    "multiblock_fp8": dict(seed=12, T=2500, H=1408, K=8, E=64, R=8, cap=None,
+                           dtype=synth.FP8_E4M3, mask_p=0.03),
+    "k1": dict(seed=13, T=777, H=256, K=1, E=16, R=4, cap=None, dtype=synth.BF16),
+    "k32_e1024": dict(seed=14, T=300, H=128, K=32, E=1024, R=8, cap=None,
+                      dtype=synth.FP8_E4M3),
+    "e_eq_r": dict(seed=15, T=200, H=384, K=4, E=16, R=16, cap=None, dtype=synth.FP8_E4M3),
+    "one_expert": dict(seed=16, T=5000, H=64, K=1, E=1, R=1, cap=None, dtype=synth.BF16),
+    "duplicates": dict(seed=17, T=900, H=512, K=8, E=5, R=5, cap=None, dtype=synth.BF16,
+                       distinct=False),
+    "t1": dict(seed=18, T=1, H=7168, K=8, E=256, R=8, cap=1, dtype=synth.FP8_E4M3),
+    "h8": dict(seed=19, T=50, H=8, K=2, E=4, R=2, cap=None, dtype=synth.BF16),
+    "tiny_values": dict(seed=20, T=64, H=256, K=4, E=8, R=2, cap=None, dtype=synth.FP8_E4M3,
+                        scale=1e-30),
+    "huge_values": dict(seed=21, T=64, H=256, K=4, E=8, R=2, cap=None, dtype=synth.FP8_E4M3,
+                        scale=1e30),
+    "large_t": dict(seed=22, T=40000, H=128, K=8, E=128, R=8, cap=None, dtype=synth.BF16,
+                    mask_p=0.01),
+}
+
+
+@functools.lru_cache(maxsize=None)
+def random_case(key):
+    return synth.make_random_case(**RANDOM[key])
+
+
+def all_cases():
+    return [pytest.param(n, id=n) for n in NAMED] + [pytest.param("r:" + k, id=k) for k in RANDOM]
+
+
+def get_case(key):
+    return random_case(key[2:]) if key.startswith("r:") else named(key)
+
+
+def full_path(c, d):
+    """layout -> dispatch -> combine through the C ABI; returns every output."""
+    lay = run_layout(d)
+    recv, scales, src_idx = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, c.dtype)
+    eo_host, eo = expert_out_dev(c, c.seed)
+    y = moedc.combine(eo, d.topk_idx, lay.slot, d.topk_weights, status=lay.status)
+    torch.cuda.synchronize()
+    return lay, recv, scales, src_idx, eo_host, y
+
+
+@pytest.mark.parametrize("key", all_cases())
+def test_parity(key):
+    c = get_case(key)
+    d = DevCase(c)
+    lay, recv, scales, src_idx, eo_host, y = full_path(c, d)
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    compare_layout(lay, ref_lay, c.T)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap,
+                            fp8=c.dtype == synth.FP8_E4M3)
+    compare_dispatch(c, recv, scales, src_idx, ref_lay, ref_d)
+    ref_c = oracle.combine(eo_host, c.topk_idx, ref_lay["slot"], c.topk_weights)
+    compare_combine(y, ref_c["y"])
+
+
+@pytest.mark.parametrize("key", [pytest.param(n, id=n) for n in
+                                 ["tiny", "low4", "low8", "low16", "default_ll"]] +
+                         [pytest.param("r:" + k, id=k) for k in
+                          ["k1", "e_eq_r", "t1", "h8", "duplicates"]])
+def test_fused_layout_dispatch_matches_oracle(key):
+    c = get_case(key)
+    d = DevCase(c)
+    lay, recv, scales, src_idx = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, c.dtype)
+    torch.cuda.synchronize()
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    compare_layout(lay, ref_lay, c.T)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap,
+                            fp8=c.dtype == synth.FP8_E4M3)
+    compare_dispatch(c, recv, scales, src_idx, ref_lay, ref_d)
+
+
+@pytest.mark.parametrize("key", ["r:multiblock_fp8", "throughput"])
+def test_layout_dispatch_large_t_uses_two_step_path(key):
+    c = get_case(key)
+    d = DevCase(c)
+    lay, recv, scales, src_idx = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, c.dtype)
+    lay2 = run_layout(d)
+    recv2, scales2, src2 = moedc.dispatch(d.x, d.topk_idx, lay2, c.E, c.cap, c.dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(lay.slot, lay2.slot)
+    assert torch.equal(src_idx, src2)
+    rows = torch.from_numpy(np.nonzero(src2.cpu().numpy().reshape(-1) >= 0)[0]).cuda()
+    a = recv.reshape(c.E * c.cap, c.H).index_select(0, rows)
+    b = recv2.reshape(c.E * c.cap, c.H).index_select(0, rows)
+    assert np.array_equal(bits_host(a), bits_host(b))
+
+
+def test_all_masked_and_empty():
+    # every entry masked: zero counts, -1 slots, y == +0
+    c = synth.make_random_case(30, T=40, H=256, K=4, E=8, R=4, cap=4, dtype=synth.BF16)
+    c.topk_idx[:] = -1
+    d = DevCase(c)
+    lay, recv, scales, src_idx, eo_host, y = full_path(c, d)
+    assert (lay.num_tokens_per_expert.cpu().numpy() == 0).all()
+    assert (lay.slot.cpu().numpy() == -1).all()
+    assert (src_idx.cpu().numpy() == -1).all()
+    assert (bits_host(y) == 0).all()
+    # T == 0: counts are written as zeros, nothing else happens
+    e = synth.make_random_case(31, T=0, H=128, K=4, E=8, R=2, cap=1, dtype=synth.FP8_E4M3)
+    de = DevCase(e)
+    lay = run_layout(de)
+    torch.cuda.synchronize()
+    assert (lay.num_tokens_per_expert.cpu().numpy() == 0).all()
+    assert (lay.num_tokens_per_rank.cpu().numpy() == 0).all()
+    lay2, recv2, sc2, src2 = moedc.layout_dispatch(de.x, de.topk_idx, e.E, e.R, e.cap, e.dtype)
+    torch.cuda.synchronize()
+    assert (src2.cpu().numpy() == -1).all()
+
+
+def test_capacity_overflow_status_and_drop():
+    c = synth.make_random_case(32, T=600, H=256, K=4, E=8, R=2, cap=None, dtype=synth.FP8_E4M3)
+    c.cap = max(1, c.cap - 20)          # too small on purpose
+    d = DevCase(c)
+    lay, recv, scales, src_idx, eo_host, y = full_path(c, d)
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    assert ref_lay["status"] == oracle.ERR_CAPACITY
+    compare_layout(lay, ref_lay, c.T)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap, fp8=True)
+    compare_dispatch(c, recv, scales, src_idx, ref_lay, ref_d)
+    ref_c = oracle.combine(eo_host, c.topk_idx, ref_lay["slot"], c.topk_weights)
+    compare_combine(y, ref_c["y"])
+
+
+@pytest.mark.parametrize("T", [7, 3000])
+def test_expert_range_status(T):
+    c = synth.make_random_case(33, T=T, H=128, K=4, E=8, R=2, cap=None, dtype=synth.BF16)
+    c.topk_idx[0, 1] = 8
+    c.topk_idx[T - 1, 3] = -5
+    d = DevCase(c)
+    lay, recv, scales, src_idx, eo_host, y = full_path(c, d)
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    assert ref_lay["status"] == oracle.ERR_EXPERT_RANGE
+    compare_layout(lay, ref_lay, c.T)
+    ref_c = oracle.combine(eo_host, c.topk_idx, ref_lay["slot"], c.topk_weights)
+    compare_combine(y, ref_c["y"])
+
+
+def test_host_argument_errors_launch_nothing():
+    c = named("tiny")
+    d = DevCase(c)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(c.E, dtype=torch.int32, device="cuda")
+    rk = torch.zeros(c.R, dtype=torch.int32, device="cuda")
+    inr = torch.zeros((c.T, c.R), dtype=torch.uint8, device="cuda")
+    sl = torch.zeros((c.T, c.K), dtype=torch.int32, device="cuda")
+    # E % R != 0, K too large, E too large, null counts
+    assert moedc.moedc_layout(d.topk_idx, c.T, c.K, 30, 4, c.cap, cnt, rk, inr, sl, None, 0, st) \
+        == moedc.ERR_ARG
+    assert moedc.moedc_layout(d.topk_idx, c.T, 33, c.E, c.R, c.cap, cnt, rk, inr, sl, None, 0,
+                              st) == moedc.ERR_ARG
+    assert moedc.moedc_layout(d.topk_idx, c.T, c.K, 2048, 4, c.cap, cnt, rk, inr, sl, None, 0,
+                              st) == moedc.ERR_ARG
+    assert moedc.moedc_layout(d.topk_idx, c.T, c.K, c.E, c.R, c.cap, None, rk, inr, sl, None, 0,
+                              st) == moedc.ERR_ARG
+    # a multi-block layout without its workspace
+    big = synth.make_random_case(34, T=4096, H=128, K=8, E=64, R=8, cap=None, dtype=synth.BF16)
+    db = DevCase(big)
+    assert moedc.moedc_layout_workspace_bytes(4096, 8, 64, 8) > 0
+    assert moedc.moedc_layout(db.topk_idx, 4096, 8, 64, 8, big.cap, cnt, rk, inr, sl, None, 0,
+                              st) == moedc.ERR_ARG
+    # fp8 with H % 128 != 0, misaligned x, missing scales
+    recv = torch.empty((c.E, c.cap, 2048), dtype=torch.uint8, device="cuda")
+    src = torch.empty((c.E, c.cap), dtype=torch.int32, device="cuda")
+    assert moedc.moedc_dispatch(d.x, c.T, 2040, d.topk_idx, sl, cnt, c.K, c.E, c.cap,
+                                moedc.FP8_E4M3, recv, None, src, st) == moedc.ERR_ARG
+    xs = d.x.view(-1)[1:]
+    assert moedc.load().moedc_dispatch(xs.data_ptr(), c.T, 2040, d.topk_idx.data_ptr(),
+                                       sl.data_ptr(), cnt.data_ptr(), c.K, c.E, c.cap,
+                                       moedc.BF16, recv.data_ptr(), None, src.data_ptr(),
+                                       st.data_ptr(), None) == moedc.ERR_ARG
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0          # nothing ran
+    assert (cnt.cpu().numpy() == 0).all()
+
+
+def test_unfilled_rows_untouched():
+    """Canary: rows past each expert's count keep the caller's bytes."""
+    c = named("low8")
+    d = DevCase(c)
+    lay = run_layout(d)
+    recv, scales, src_idx = moedc.alloc_recv(c.E, c.cap, c.H, c.dtype, "cuda")
+    recv.view(torch.uint8).fill_(0xAB)
+    scales.view(torch.int32).fill_(-1)
+    moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, c.dtype, out=(recv, scales, src_idx))
+    torch.cuda.synchronize()
+    cnt = lay.num_tokens_per_expert.cpu().numpy()
+    r = bits_host(recv)
+    s = scales.view(torch.int32).cpu().numpy()
+    for e in range(c.E):
+        assert (r[e, cnt[e]:] == 0xAB).all()
+        assert (s[e, cnt[e]:] == -1).all()
+
+
+def test_graph_replay_bit_exact_with_eager():
+    """Layout + dispatch + combine captured in a CUDA graph and replayed give
+    the eager bytes (all buffers caller-owned, nothing allocated per call)."""
+    c = named("default_ll")
+    d = DevCase(c)
+    eo_host, eo = expert_out_dev(c, 0)
+    dev = "cuda"
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(c.E, dtype=torch.int32, device=dev)
+    rk = torch.empty(c.R, dtype=torch.int32, device=dev)
+    inr = torch.empty((c.T, c.R), dtype=torch.uint8, device=dev)
+    sl = torch.empty((c.T, c.K), dtype=torch.int32, device=dev)
+    recv, scales, src = moedc.alloc_recv(c.E, c.cap, c.H, c.dtype, dev)
+    y = torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev)
+    ws = moedc.layout_workspace(c.T, c.K, c.E, c.R, dev)
+    wsb = 0 if ws is None else ws.numel()
+
+    def step(stream=None):
+        assert moedc.moedc_layout_dispatch(d.x, d.topk_idx, c.T, c.H, c.K, c.E, c.R, c.cap,
+                                           c.dtype, cnt, rk, inr, sl, recv, scales, src, ws, wsb,
+                                           st, stream) == moedc.OK
+        assert moedc.moedc_combine(eo, c.E, c.cap, c.H, d.topk_idx, sl, d.topk_weights, c.T,
+                                   c.K, y, st, stream) == moedc.OK
+
+    step()
+    torch.cuda.synchronize()
+    eager = [bits_host(t).copy() for t in (cnt, rk, inr, sl, src, y)] + \
+        [bits_host(recv).copy(), scales.cpu().numpy().copy()]
+    for t in (cnt, rk, sl, src, y, scales):
+        t.zero_()
+    recv.view(torch.uint8).zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    again = [bits_host(t) for t in (cnt, rk, inr, sl, src, y)] + \
+        [bits_host(recv), scales.cpu().numpy()]
+    for a, b in zip(eager, again):
+        np.testing.assert_array_equal(a, b)
+    assert int(st.item()) == 0
+
+
+def test_runs_on_a_side_stream():
+    c = named("tiny")
+    d = DevCase(c)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        lay, recv, scales, src_idx = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap,
+                                                           c.dtype)
+    s.synchronize()
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    compare_layout(lay, ref_lay, c.T)
