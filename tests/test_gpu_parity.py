@@ -250,10 +250,15 @@ def test_graph_replay_bit_exact_with_eager():
         assert moedc.moedc_combine(eo, c.E, c.cap, c.H, d.topk_idx, sl, d.topk_weights, c.T,
                                    c.K, y, st, stream) == moedc.OK
 
+    def filled_rows():
+        rows = torch.nonzero(src.reshape(-1) >= 0).reshape(-1)
+        return [bits_host(recv.reshape(c.E * c.cap, c.H).index_select(0, rows)),
+                scales.reshape(c.E * c.cap, c.G).index_select(0, rows).cpu().numpy()]
+
     step()
     torch.cuda.synchronize()
-    eager = [bits_host(t).copy() for t in (cnt, rk, inr, sl, src, y)] + \
-        [bits_host(recv).copy(), scales.cpu().numpy().copy()]
+    # rows no entry reaches are never written, so only filled rows are compared
+    eager = [bits_host(t).copy() for t in (cnt, rk, inr, sl, src, y)] + filled_rows()
     for t in (cnt, rk, sl, src, y, scales):
         t.zero_()
     recv.view(torch.uint8).zero_()
@@ -266,8 +271,7 @@ def test_graph_replay_bit_exact_with_eager():
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    again = [bits_host(t) for t in (cnt, rk, inr, sl, src, y)] + \
-        [bits_host(recv), scales.cpu().numpy()]
+    again = [bits_host(t) for t in (cnt, rk, inr, sl, src, y)] + filled_rows()
     for a, b in zip(eager, again):
         np.testing.assert_array_equal(a, b)
     assert int(st.item()) == 0
