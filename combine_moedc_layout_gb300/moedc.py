@@ -31,7 +31,10 @@ BF16 = 0
 FP8_E4M3 = 1
 
 EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes",
-            "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch")
+            "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
+            "moedc_layout_static_scratch")
+
+STATIC_SCRATCH_BYTES = 1 << 20   # MOEDC_STATIC_SCRATCH_BYTES
 
 _lib = None
 
@@ -72,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_layout_dispatch.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, Z,
                                           P, P]
     lib.moedc_layout_dispatch.restype = I
+    lib.moedc_layout_static_scratch.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P]
+    lib.moedc_layout_static_scratch.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -111,6 +116,17 @@ def moedc_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert, num_tokens_pe
     return load().moedc_layout(_p(topk_idx), T, K, E, R, cap, _p(num_tokens_per_expert),
                                _p(num_tokens_per_rank), _p(is_token_in_rank), _p(slot),
                                _p(workspace), workspace_bytes, _p(dev_status), _stream(stream))
+
+
+def moedc_layout_static_scratch(topk_idx, T, K, E, R, cap, num_tokens_per_expert,
+                                num_tokens_per_rank, is_token_in_rank, slot, dev_status,
+                                stream=None) -> int:
+    """moedc_layout without a workspace: for callers that cannot allocate
+    device memory, the library's own fixed-size device array serves as
+    scratch.  Calls that overlap on the GPU race on that array."""
+    return load().moedc_layout_static_scratch(
+        _p(topk_idx), T, K, E, R, cap, _p(num_tokens_per_expert), _p(num_tokens_per_rank),
+        _p(is_token_in_rank), _p(slot), _p(dev_status), _stream(stream))
 
 
 def moedc_dispatch(x, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, out_dtype, recv,

@@ -129,6 +129,29 @@ MOEDC_EXPORT int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int 
                  int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * moedc_layout for callers that cannot allocate device memory: no workspace
+ * argument, the scratch lives in a fixed array inside the library.  The pages
+ * have no counterpart to this entry point; it exists for hosts with no device
+ * allocator of their own, plugins inside a framework whose memory pool owns
+ * the GPU, and serving loops that may not call cudaMalloc after start-up.
+ * Same arguments, results and data errors as moedc_layout, except:
+ *  - shapes whose moedc_layout_workspace_bytes() exceeds
+ *    MOEDC_STATIC_SCRATCH_BYTES return MOEDC_ERR_ARG and launch nothing;
+ *  - the array (MOEDC_STATIC_SCRATCH_BYTES per device) stays resident on every
+ *    GPU that loads the library until the process exits;
+ *  - the first call on a device looks up the array's device address and
+ *    caches it; make that first call before any stream capture begins;
+ *  - all calls share the array, so calls that overlap on the GPU race and
+ *    give wrong results: order them on one stream.
+ * The call allocates nothing and calls no allocating routine.
+ */
+#define MOEDC_STATIC_SCRATCH_BYTES (1u << 20)
+MOEDC_EXPORT int moedc_layout_static_scratch(const int32_t* topk_idx, int T, int K, int E,
+                 int R, int cap, int32_t* num_tokens_per_expert,
+                 int32_t* num_tokens_per_rank, uint8_t* is_token_in_rank, int32_t* slot,
+                 int32_t* dev_status, cudaStream_t stream);
+
+/*
  * Dispatch [DEEPEP693 Summary; MORI614 DispatchIntraNode note].
  * For every entry (t, k) with expert e in [0, E) and slot s in [0, cap):
  *   src_idx[e][s] = t
