@@ -78,9 +78,10 @@ inline int launch_status() { return cudaGetLastError() == cudaSuccess ? MOEDC_OK
 
 // Layout geometry: tokens per thread block of the layout kernels.
 struct LayoutGeom {
-    int tpc;        // tokens per block
+    bool sweep;     // single-launch sweep path (no scratch)
+    int tpc;        // blocked path: tokens per block
     int blocks;     // number of blocks (>= 1)
-    size_t ws;      // workspace bytes (0 when blocks == 1)
+    size_t ws;      // scratch bytes (0 on the sweep path)
 };
 LayoutGeom layout_geometry(int T, int K, int E, int R);
 bool layout_args_ok(int T, int K, int E, int R, int cap);

@@ -10,47 +10,165 @@
 // note: the topk loads are issued together and a negative sentinel expert is
 // tested before any division).
 //
-// Two kernels, no atomics that decide order:
-//   count  (skipped when one block holds every token): block c histograms its
-//          contiguous run of tokens into workspace row c, and counts the
-//          distinct tokens it sends to each rank.
-//   assign: block c turns the rows of blocks < c into per-expert base offsets,
-//          splits its own run over 8 warps (per-warp counts + a scan across
-//          warps), then each warp walks its entries in order and ranks equal
-//          experts inside a 32-entry tile with __match_any_sync.  The last
-//          block also writes the totals.
+// No atomics decide order.  Two paths, picked by the number of entries:
+//
+// Sweep (T*K <= kSweepMaxEntries, one launch, no scratch): block e < E owns
+//   expert e and reads every entry (the whole top-k table is at most 256 KB
+//   and stays in L2); a block-wide exclusive scan over per-thread match
+//   counts gives each match its slot in (t, k) order.  Block E + r owns rank
+//   r: it writes column r of is_token_in_rank and counts its tokens.  No
+//   block waits on another.
+//
+// Blocked (larger T*K, two launches, caller scratch):
+//   count:  block c histograms its contiguous run of tokens into scratch row
+//           c, and counts the distinct tokens it sends to each rank.
+//   assign: block c turns the rows of blocks < c into per-expert base
+//           offsets, splits its own run over 8 warps (per-warp counts + a
+//           scan across warps), then each warp walks its entries in order and
+//           ranks equal experts inside a 32-entry tile with __match_any_sync.
+//           The last block also writes the totals.
+// Rank membership is a range test lo <= e < lo + E/R (no division).
 #include "common.cuh"
 
 namespace moedc {
 
 constexpr int kLayoutThreads = 256;
 constexpr int kLayoutWarps = kLayoutThreads / kWarp;
-constexpr int kEntriesPerBlock = 1024;     // target (token, k) entries per block
-constexpr int kSingleBlockEntries = 2048;  // up to here one block does everything
+constexpr int kEntriesPerBlock = 1024;     // blocked path: (token, k) entries per block
 constexpr int kMaxLayoutBlocks = 1024;
+constexpr int kSweepThreads = 1024;
+constexpr int kSweepWarps = kSweepThreads / kWarp;
+constexpr int kSweepV = 16;                // consecutive entries per thread per round
+constexpr int kSweepMaxEntries = 65536;    // sweep path up to here
 
 __device__ __forceinline__ bool valid_expert(int e, int E) { return e >= 0 && e < E; }
 
-// does token row `row` (K entries in shared memory) send anything to rank r?
-__device__ __forceinline__ bool token_in_rank(const int32_t* row, int K, int E, int epr, int r)
+// does token row `row` (K entries) send anything to the rank owning [lo, lo + epr)?
+__device__ __forceinline__ bool token_in_rank(const int32_t* row, int K, int lo, int epr)
 {
     for (int k = 0; k < K; ++k) {
-        int e = row[k];
-        if (valid_expert(e, E) && e / epr == r)
-            return true;
+        const unsigned d = (unsigned)row[k] - (unsigned)lo;
+        if (d < (unsigned)epr) return true;
     }
     return false;
 }
 
-// is entry k the first of its token row that goes to rank r?
-__device__ __forceinline__ bool first_in_rank(const int32_t* row, int k, int E, int epr, int r)
+// is entry k the first of its token row that goes to the rank owning [lo, lo + epr)?
+__device__ __forceinline__ bool first_in_rank(const int32_t* row, int k, int lo, int epr)
 {
     for (int j = 0; j < k; ++j) {
-        int e = row[j];
-        if (valid_expert(e, E) && e / epr == r)
-            return false;
+        const unsigned d = (unsigned)row[j] - (unsigned)lo;
+        if (d < (unsigned)epr) return false;
     }
     return true;
+}
+
+// Sweep layout: blocks [0, E) are experts, blocks [E, E + R) are ranks.
+__global__ void __launch_bounds__(kSweepThreads)
+layout_sweep_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, int R, int cap,
+                    bool vec_ok, int32_t* __restrict__ num_tokens_per_expert,
+                    int32_t* __restrict__ num_tokens_per_rank,
+                    uint8_t* __restrict__ is_token_in_rank, int32_t* __restrict__ slot,
+                    int32_t* __restrict__ status)
+{
+    __shared__ int32_t s_warp[kSweepWarps];
+    __shared__ int32_t s_total;
+    const int tid = threadIdx.x;
+    const int lane = tid % kWarp;
+    const int warp = tid / kWarp;
+    const int n = T * K;
+
+    if (blockIdx.x < E) {
+        const int target = blockIdx.x;
+        const bool sweeper = (blockIdx.x == 0);   // block 0 also marks invalid entries
+        bool bad = false;
+        int running = 0;
+        for (int base = 0; base < n; base += kSweepThreads * kSweepV) {
+            const int i0 = base + tid * kSweepV;
+            int v[kSweepV];
+            if (vec_ok && i0 + kSweepV <= n) {
+                const int4* p = reinterpret_cast<const int4*>(topk_idx + i0);
+#pragma unroll
+                for (int q = 0; q < kSweepV / 4; ++q) {
+                    const int4 w = __ldg(p + q);
+                    v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kSweepV; ++j)
+                    v[j] = (i0 + j < n) ? __ldg(topk_idx + i0 + j) : -1;
+            }
+            unsigned m = 0;
+#pragma unroll
+            for (int j = 0; j < kSweepV; ++j) m |= (v[j] == target ? 1u : 0u) << j;
+            if (sweeper) {
+#pragma unroll
+                for (int j = 0; j < kSweepV; ++j) {
+                    if (i0 + j < n && !valid_expert(v[j], E)) {
+                        slot[i0 + j] = -1;
+                        if (v[j] != -1) bad = true;
+                    }
+                }
+            }
+            // block-wide exclusive scan of the per-thread match counts
+            const int c = __popc(m);
+            int incl = c;
+#pragma unroll
+            for (int d = 1; d < kWarp; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (lane == kWarp - 1) s_warp[warp] = incl;
+            __syncthreads();
+            if (warp == 0) {
+                const int wv = s_warp[lane];
+                int wi = wv;
+#pragma unroll
+                for (int d = 1; d < kWarp; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, wi, d);
+                    if (lane >= d) wi += y;
+                }
+                s_warp[lane] = wi - wv;
+                if (lane == kWarp - 1) s_total = wi;
+            }
+            __syncthreads();
+            int s = running + s_warp[warp] + incl - c;
+            while (m) {
+                const int j = __ffs(m) - 1;
+                m &= m - 1;
+                slot[i0 + j] = s++;
+            }
+            running += s_total;
+            __syncthreads();   // s_warp / s_total are rewritten next round
+        }
+        if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+        if (tid == 0) {
+            num_tokens_per_expert[target] = running;
+            if (running > cap) raise_status(status, MOEDC_ERR_CAPACITY);
+        }
+        return;
+    }
+
+    // rank block: column r of is_token_in_rank and its token count
+    const int r = blockIdx.x - E;
+    const int epr = E / R;
+    const int lo = r * epr;
+    int c = 0;
+    for (int t = tid; t < T; t += kSweepThreads) {
+        const bool in = token_in_rank(topk_idx + (int64_t)t * K, K, lo, epr);
+        is_token_in_rank[(int64_t)t * R + r] = in ? 1 : 0;
+        c += in ? 1 : 0;
+    }
+#pragma unroll
+    for (int d = kWarp / 2; d > 0; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    if (lane == 0) s_warp[warp] = c;
+    __syncthreads();
+    if (warp == 0) {
+        int v = s_warp[lane];
+#pragma unroll
+        for (int d = kWarp / 2; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+        if (lane == 0) num_tokens_per_rank[r] = v;
+    }
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
@@ -83,7 +201,7 @@ layout_count_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, i
         atomicAdd(&s_hist[e], 1);
         const int k = i % K;
         const int r = e / epr;
-        if (first_in_rank(s_idx + (i - k), k, E, epr, r))
+        if (first_in_rank(s_idx + (i - k), k, r * epr, epr))
             atomicAdd(&s_rank[r], 1);
     }
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
@@ -141,7 +259,7 @@ layout_assign_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, 
             if (!valid_expert(e, E)) { bad = true; continue; }
             const int k = i % K;
             const int r = e / epr;
-            if (first_in_rank(s_idx + (i - k), k, E, epr, r))
+            if (first_in_rank(s_idx + (i - k), k, r * epr, epr))
                 atomicAdd(&s_rank[r], 1);
         }
         if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
@@ -197,7 +315,7 @@ layout_assign_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, 
     for (int b = threadIdx.x; b < nt * R; b += blockDim.x) {
         const int t = b / R;
         const int r = b - t * R;
-        rows[b] = token_in_rank(s_idx + t * K, K, E, epr, r) ? 1 : 0;
+        rows[b] = token_in_rank(s_idx + t * K, K, r * epr, epr) ? 1 : 0;
     }
 }
 
@@ -225,12 +343,14 @@ LayoutGeom layout_geometry(int T, int K, int E, int R)
 {
     LayoutGeom g{};
     const int64_t n = (int64_t)T * K;
-    if (n <= moedc::kSingleBlockEntries) {
+    if (n <= moedc::kSweepMaxEntries) {
+        g.sweep = true;
         g.tpc = T;
-        g.blocks = 1;
+        g.blocks = E + R;
         g.ws = 0;
         return g;
     }
+    g.sweep = false;
     int tpc = (moedc::kEntriesPerBlock + K - 1) / K;
     const int min_tpc = (T + moedc::kMaxLayoutBlocks - 1) / moedc::kMaxLayoutBlocks;
     if (tpc < min_tpc) tpc = min_tpc;
@@ -255,6 +375,13 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
                   int32_t* dev_status, cudaStream_t stream)
 {
     const LayoutGeom g = layout_geometry(T, K, E, R);
+    if (g.sweep) {
+        const bool vec_ok = aligned(topk_idx, 16);
+        moedc::layout_sweep_kernel<<<g.blocks, moedc::kSweepThreads, 0, stream>>>(
+            topk_idx, T, K, E, R, cap, vec_ok, num_tokens_per_expert, num_tokens_per_rank,
+            is_token_in_rank, slot, dev_status);
+        return launch_status();
+    }
     int32_t* ws_hist = static_cast<int32_t*>(workspace);
     int32_t* ws_rank = ws_hist ? ws_hist + (size_t)g.blocks * E : nullptr;
     if (g.blocks > 1) {

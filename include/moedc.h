@@ -101,7 +101,8 @@ MOEDC_EXPORT const char* moedc_strerror(int code);
 
 /*
  * Bytes of device scratch that moedc_layout / moedc_layout_dispatch need for
- * this shape (0 when the whole layout fits one thread block).  The caller
+ * this shape (0 when T * K <= 65536: that layout is one launch without
+ * scratch).  The caller
  * allocates it (any 16-byte aligned device buffer of at least this size) and
  * may reuse it across calls that are ordered on one stream.  Returns 0 for
  * arguments that the layout would reject.

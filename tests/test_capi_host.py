@@ -56,11 +56,14 @@ def test_version_and_strerror(lib):
 
 
 def test_workspace_bytes(lib):
-    # one block handles up to 2048 entries: no scratch
+    # up to 65536 entries the layout is a single launch without scratch
     assert moedc.moedc_layout_workspace_bytes(64, 4, 32, 4) == 0
     assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == 0
-    # 4096 x 8 entries: 128 tokens per block -> 32 blocks x (E + R) int32
-    assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 32 * (256 + 8) * 4
+    assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 0
+    assert moedc.moedc_layout_workspace_bytes(8192, 8, 256, 8) == 0
+    # beyond: 128 tokens per block -> blocks x (E + R) int32
+    assert moedc.moedc_layout_workspace_bytes(8193, 8, 256, 8) == 65 * (256 + 8) * 4
+    assert moedc.moedc_layout_workspace_bytes(40000, 8, 128, 8) == 313 * (128 + 8) * 4
     # rejected shapes report 0
     assert moedc.moedc_layout_workspace_bytes(4096, 8, 250, 8) == 0
     assert moedc.moedc_layout_workspace_bytes(4096, 0, 256, 8) == 0
@@ -89,8 +92,8 @@ def test_argument_errors_return_before_cuda(lib):
         moedc.ERR_ARG
     assert lib.moedc_combine(fake, 8, 4, 128, fake, fake, fake, 4, 2, None, fake, None) == \
         moedc.ERR_ARG
-    # fused: multi-block shape without workspace
-    assert lib.moedc_layout_dispatch(fake, fake, 4096, 256, 8, 64, 8, 600, moedc.BF16, fake,
+    # fused: a shape past the single-launch layout (> 65536 entries) without workspace
+    assert lib.moedc_layout_dispatch(fake, fake, 9000, 256, 8, 64, 8, 1200, moedc.BF16, fake,
                                      fake, fake, fake, fake, None, fake, None, 0, fake,
                                      None) == moedc.ERR_ARG
 

@@ -187,14 +187,19 @@ def test_host_argument_errors_launch_nothing():
                               st) == moedc.ERR_ARG
     assert moedc.moedc_layout(d.topk_idx, c.T, c.K, c.E, c.R, c.cap, None, rk, inr, sl, None, 0,
                               st) == moedc.ERR_ARG
-    # a multi-block layout without its workspace
-    big = synth.make_random_case(34, T=4096, H=128, K=8, E=64, R=8, cap=None, dtype=synth.BF16)
+    # a layout past the single-launch size (> 65536 entries) without its workspace;
+    # full-size outputs, so nothing could go out of bounds even if it launched
+    big = synth.make_random_case(34, T=9000, H=128, K=8, E=64, R=8, cap=None, dtype=synth.BF16)
     db = DevCase(big)
-    assert moedc.moedc_layout_workspace_bytes(4096, 8, 64, 8) > 0
-    assert moedc.moedc_layout(db.topk_idx, 4096, 8, 64, 8, big.cap, cnt, rk, inr, sl, None, 0,
-                              st) == moedc.ERR_ARG
+    assert moedc.moedc_layout_workspace_bytes(9000, 8, 64, 8) > 0
+    bcnt = torch.full((64,), -7, dtype=torch.int32, device="cuda")
+    brk = torch.zeros(8, dtype=torch.int32, device="cuda")
+    binr = torch.zeros((9000, 8), dtype=torch.uint8, device="cuda")
+    bsl = torch.zeros((9000, 8), dtype=torch.int32, device="cuda")
+    assert moedc.moedc_layout(db.topk_idx, 9000, 8, 64, 8, big.cap, bcnt, brk, binr, bsl, None,
+                              0, st) == moedc.ERR_ARG
     # fp8 with H % 128 != 0, misaligned x, missing scales
-    recv = torch.empty((c.E, c.cap, 2048), dtype=torch.uint8, device="cuda")
+    recv = torch.empty((c.E, c.cap, 2048), dtype=torch.bfloat16, device="cuda")  # fits either
     src = torch.empty((c.E, c.cap), dtype=torch.int32, device="cuda")
     assert moedc.moedc_dispatch(d.x, c.T, 2040, d.topk_idx, sl, cnt, c.K, c.E, c.cap,
                                 moedc.FP8_E4M3, recv, None, src, st) == moedc.ERR_ARG
@@ -206,6 +211,7 @@ def test_host_argument_errors_launch_nothing():
     torch.cuda.synchronize()
     assert int(st.item()) == 0          # nothing ran
     assert (cnt.cpu().numpy() == 0).all()
+    assert (bcnt.cpu().numpy() == -7).all()
 
 
 def test_unfilled_rows_untouched():

@@ -51,8 +51,10 @@ def _same(a, b):
 
 
 CASES = [
-    # the 4096-token workload: several layout blocks, so the scratch is used
-    lambda: synth.make_case("throughput"),
+    # more than 65536 (token, k) entries: the layout runs its two-kernel path,
+    # which is the one that needs scratch
+    lambda: synth.make_random_case(40, T=12000, H=128, K=8, E=256, R=8, cap=None,
+                                   dtype=synth.BF16),
     # more tokens, masked entries, different expert / rank counts
     lambda: synth.make_random_case(41, T=40000, H=128, K=8, E=128, R=8, cap=None,
                                    dtype=synth.BF16, mask_p=0.02),
@@ -73,9 +75,11 @@ def test_static_scratch_matches_workspace_entry_point_twice_in_a_row():
 
 
 def test_static_scratch_second_call_not_polluted_by_first():
-    a = synth.make_random_case(42, T=6000, H=128, K=8, E=256, R=8, cap=None, dtype=synth.BF16)
-    b = synth.make_random_case(43, T=5000, H=128, K=6, E=64, R=4, cap=None, dtype=synth.BF16,
+    a = synth.make_random_case(42, T=9000, H=128, K=8, E=256, R=8, cap=None, dtype=synth.BF16)
+    b = synth.make_random_case(43, T=12000, H=128, K=6, E=64, R=4, cap=None, dtype=synth.BF16,
                                mask_p=0.1)
+    for c in (a, b):
+        assert moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R) > 0
     ia = torch.from_numpy(a.topk_idx).cuda()
     ib = torch.from_numpy(b.topk_idx).cuda()
     got_a = _static(ia, a.T, a.K, a.E, a.R, a.cap)
