@@ -47,16 +47,22 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every csrc/*.cu and link libmoedc.so; returns its path."""
-    if not force and not extra_flags and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile every csrc/*.cu and link libmoedc.so; returns its path.
+
+    extra_flags / out_dir build a variant (for example with a tuning macro
+    set by -D) into another directory without touching the default library."""
+    if not force and not extra_flags and out_dir is None and up_to_date():
         return LIB_PATH
-    os.makedirs(OUT_DIR, exist_ok=True)
+    OUT_DIR_ = out_dir or OUT_DIR
+    LIB_PATH_ = os.path.join(OUT_DIR_, "libmoedc.so")
+    os.makedirs(OUT_DIR_, exist_ok=True)
     nvcc = _nvcc()
     flags = ARCH + NVCC_FLAGS + (extra_flags or []) + ["-I" + INCLUDE, "-I" + CSRC]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR_, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,13 +73,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    tmp = LIB_PATH_ + f".{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, LIB_PATH_)
+    return LIB_PATH_
 
 
 if __name__ == "__main__":

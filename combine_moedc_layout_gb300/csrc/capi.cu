@@ -1,4 +1,6 @@
-// Entry points that launch nothing: version, status text, device query.
+// Entry points that launch nothing: version, status text, device queries.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moedc_host {
@@ -18,6 +20,36 @@ int sm_count()
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+int resident_blocks(const void* kernel, int threads, size_t smem)
+{
+    // blocks of `kernel` that fit on the whole device at once (occupancy x
+    // SMs), cached per kernel and device; grid-strided kernels launch at most
+    // this many so that no block waits for a second wave
+    struct Entry {
+        const void* kernel;
+        int dev, threads;
+        size_t smem;
+        int blocks;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].kernel == kernel && cache[i].dev == dev && cache[i].threads == threads &&
+            cache[i].smem == smem)
+            return cache[i].blocks;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+            cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int blocks = per_sm * sm_count();
+    if (used < 64) cache[used++] = Entry{kernel, dev, threads, smem, blocks};
+    return blocks;
 }
 
 }  // namespace moedc_host

@@ -8,13 +8,27 @@
 // staged).  The kernel is an HBM read stream: K gathered rows per token.
 #include "common.cuh"
 
+// Tuning knobs (compile-time): 16-byte vectors per lane per gathered row,
+// rows whose loads are in flight together, and the minimum resident blocks
+// per SM the register budget must allow.
+#ifndef MOEDC_COMBINE_VEC
+#define MOEDC_COMBINE_VEC 2
+#endif
+#ifndef MOEDC_COMBINE_BATCH
+#define MOEDC_COMBINE_BATCH 8
+#endif
+#ifndef MOEDC_COMBINE_MINB
+#define MOEDC_COMBINE_MINB 2
+#endif
+
 namespace moedc {
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineSlice = 512;   // channels per warp item
-constexpr int kCombineBatch = 8;     // gathered rows in flight per lane
+constexpr int kCombineVec = MOEDC_COMBINE_VEC;
+constexpr int kCombineSlice = 256 * kCombineVec;   // channels per warp item
+constexpr int kCombineBatch = MOEDC_COMBINE_BATCH;
 
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreads, MOEDC_COMBINE_MINB)
 combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
                const float* __restrict__ topk_weights, int T, int K,
@@ -26,28 +40,41 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     bool bad = false;
 
-    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
-         item < items; item += nwarps) {
+    // routing entries of a work item: lane k < K holds entry k (expert, slot, weight)
+    auto load_routing = [&](int64_t it, int& e, int& s, float& w) {
+        e = -1; s = -1; w = 0.0f;
+        if (it < items && lane < K) {
+            const int64_t t = it / nslice;
+            e = __ldg(topk_idx + t * K + lane);
+            s = __ldg(slot + t * K + lane);
+            w = __ldg(topk_weights + t * K + lane);
+        }
+    };
+    int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+    int my_e, my_s;
+    float my_w;
+    load_routing(item, my_e, my_s, my_w);
+    for (; item < items; item += nwarps) {
         const int t = (int)(item / nslice);
         const int sl = (int)(item - (int64_t)t * nslice);
-        int my_e = -1, my_s = -1;
-        float my_w = 0.0f;
-        if (lane < K) {
-            my_e = topk_idx[(int64_t)t * K + lane];
-            my_s = slot[(int64_t)t * K + lane];
-            my_w = topk_weights[(int64_t)t * K + lane];
-            if (sl == 0 && (my_e < -1 || my_e >= E)) bad = true;
-        }
-        // lane covers channels c0 .. c0+8 and c1 .. c1+8 (each warp access is 512 B)
-        const int c0 = sl * kCombineSlice + lane * 8;
-        const int c1 = c0 + 256;
-        const bool a0 = c0 < H, a1 = c1 < H;
-        float acc[16];
+        if (sl == 0 && lane < K && (my_e < -1 || my_e >= E)) bad = true;
+        // vector v of this lane covers channels c[v] .. c[v] + 8; each warp-wide
+        // 16-byte access covers 512 contiguous bytes
+        int c[kCombineVec];
+        bool act[kCombineVec];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int v = 0; v < kCombineVec; ++v) {
+            c[v] = sl * kCombineSlice + v * 256 + lane * 8;
+            act[v] = c[v] < H;
+        }
+        float acc[8 * kCombineVec];
+#pragma unroll
+        for (int i = 0; i < 8 * kCombineVec; ++i) acc[i] = 0.0f;
+        int nx_e, nx_s;
+        float nx_w;
 
         for (int k0 = 0; k0 < K; k0 += kCombineBatch) {
-            uint4 v0[kCombineBatch], v1[kCombineBatch];
+            uint4 buf[kCombineBatch][kCombineVec];
             float wk[kCombineBatch];
             bool ok[kCombineBatch];
 #pragma unroll
@@ -57,36 +84,43 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
                 const int s = __shfl_sync(0xffffffffu, my_s, k & 31);
                 wk[j] = __shfl_sync(0xffffffffu, my_w, k & 31);
                 ok[j] = k < K && e >= 0 && e < E && s >= 0 && s < cap;
-                v0[j] = make_uint4(0, 0, 0, 0);
-                v1[j] = make_uint4(0, 0, 0, 0);
-                if (ok[j]) {
-                    const uint16_t* row = expert_out + ((int64_t)e * cap + s) * H;
-                    if (a0) v0[j] = ld_global_nc(reinterpret_cast<const uint4*>(row + c0));
-                    if (a1) v1[j] = ld_global_nc(reinterpret_cast<const uint4*>(row + c1));
+                const uint16_t* row = ok[j] ? expert_out + ((int64_t)e * cap + s) * H : expert_out;
+#pragma unroll
+                for (int v = 0; v < kCombineVec; ++v) {
+                    buf[j][v] = make_uint4(0, 0, 0, 0);
+                    if (ok[j] && act[v])
+                        buf[j][v] = ld_global_nc(reinterpret_cast<const uint4*>(row + c[v]));
                 }
             }
+            // the next item's routing travels while these rows are in flight
+            if (k0 == 0) load_routing(item + nwarps, nx_e, nx_s, nx_w);
 #pragma unroll
             for (int j = 0; j < kCombineBatch; ++j) {
                 if (!ok[j]) continue;
-                const uint32_t u[8] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w,
-                                       v1[j].x, v1[j].y, v1[j].z, v1[j].w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wk[j], bf16_lo(u[i])));
-                    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wk[j], bf16_hi(u[i])));
+                for (int v = 0; v < kCombineVec; ++v) {
+                    const uint32_t u[4] = {buf[j][v].x, buf[j][v].y, buf[j][v].z, buf[j][v].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float* a = acc + 8 * v + 2 * i;
+                        a[0] = __fadd_rn(a[0], __fmul_rn(wk[j], bf16_lo(u[i])));
+                        a[1] = __fadd_rn(a[1], __fmul_rn(wk[j], bf16_hi(u[i])));
+                    }
                 }
             }
         }
         uint16_t* yrow = y + (int64_t)t * H;
-        if (a0)
-            st_global_cs(reinterpret_cast<uint4*>(yrow + c0),
-                         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
-        if (a1)
-            st_global_cs(reinterpret_cast<uint4*>(yrow + c1),
-                         make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                    pack_bf16x2(acc[12], acc[13]),
-                                    pack_bf16x2(acc[14], acc[15])));
+#pragma unroll
+        for (int v = 0; v < kCombineVec; ++v) {
+            if (!act[v]) continue;
+            const float* a = acc + 8 * v;
+            st_global_cs(reinterpret_cast<uint4*>(yrow + c[v]),
+                         make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                    pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7])));
+        }
+        my_e = nx_e;
+        my_s = nx_s;
+        my_w = nx_w;
     }
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
 }
@@ -112,8 +146,9 @@ extern "C" int moedc_combine(const void* expert_out, int E, int cap, int H,
     const int nslice = (H + moedc::kCombineSlice - 1) / moedc::kCombineSlice;
     const int64_t items = (int64_t)T * nslice;
     int64_t blocks = (items + warps_per_block - 1) / warps_per_block;
-    const int64_t max_blocks = (int64_t)sm_count() * 8;
-    if (blocks > max_blocks) blocks = max_blocks;
+    const int64_t resident =
+        resident_blocks((const void*)moedc::combine_kernel, moedc::kCombineThreads, 0);
+    if (blocks > resident) blocks = resident;
     moedc::combine_kernel<<<(int)blocks, moedc::kCombineThreads, 0, stream>>>(
         static_cast<const uint16_t*>(expert_out), E, cap, H, topk_idx, slot, topk_weights, T, K,
         static_cast<uint16_t*>(y), dev_status);

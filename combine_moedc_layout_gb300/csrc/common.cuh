@@ -73,6 +73,8 @@ __device__ __forceinline__ void st_global_cs_f32(float* p, float v)
 namespace moedc_host {
 
 int sm_count();                 // multiprocessors of the current device
+// blocks of `kernel` resident on the whole current device at once
+int resident_blocks(const void* kernel, int threads, size_t smem);
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? MOEDC_OK : MOEDC_ERR_CUDA; }
 

@@ -11,10 +11,14 @@
 
 namespace moedc {
 
+#ifndef MOEDC_DISPATCH_MINB
+#define MOEDC_DISPATCH_MINB 4
+#endif
+
 constexpr int kDispatchThreads = 256;
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kDispatchThreads)
+__global__ void __launch_bounds__(kDispatchThreads, MOEDC_DISPATCH_MINB)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
                 const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
                 const int32_t* __restrict__ num_tokens_per_expert, int K, int E, int cap,
@@ -27,26 +31,39 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / kWarp);
     bool bad = false;
 
-    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
-         item < items; item += nwarps) {
+    // a work item's inputs: routing entry k == lane, and the lane's x vectors
+    auto load_item = [&](int64_t it, int& e, int& s, SliceX& v) {
+        e = -1;
+        s = -1;
+        v = SliceX{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (it >= items) return;
+        const int64_t t = it / nslice;
+        const int sl = (int)(it - t * nslice);
+        if (lane < K) {
+            e = __ldg(topk_idx + t * K + lane);
+            s = __ldg(slot + t * K + lane);
+        }
+        v = load_slice<kFp8>(x + t * H, H, sl, lane);
+    };
+    int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+    int my_e, my_s;
+    SliceX cur;
+    load_item(item, my_e, my_s, cur);
+    for (; item < items; item += nwarps) {
         const int t = (int)(item / nslice);
         const int sl = (int)(item - (int64_t)t * nslice);
-        int my_e = -1, my_s = -1;
-        if (lane < K) {
-            my_e = topk_idx[(int64_t)t * K + lane];
-            my_s = slot[(int64_t)t * K + lane];
-        }
+        // the next item's routing and x travel while this one is stored
+        int nx_e, nx_s;
+        SliceX nxt;
+        load_item(item + nwarps, nx_e, nx_s, nxt);
         if (sl == 0 && lane < K) {
             if (my_e < -1 || my_e >= E) bad = true;
             if (dest_ok(my_e, my_s, E, cap)) src_idx[(int64_t)my_e * cap + my_s] = t;
         }
-        const uint16_t* xrow = x + (int64_t)t * H;
-        if (kFp8)
-            dispatch_slice_fp8(xrow, H, sl, lane, K, my_e, my_s, E, cap,
-                               static_cast<uint8_t*>(recv), scales);
-        else
-            dispatch_slice_bf16(xrow, H, sl, lane, K, my_e, my_s, E, cap,
-                                static_cast<uint16_t*>(recv));
+        store_slice<kFp8>(cur, H, sl, lane, K, my_e, my_s, E, cap, recv, scales);
+        my_e = nx_e;
+        my_s = nx_s;
+        cur = nxt;
     }
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
 
@@ -95,8 +112,10 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
     int64_t blocks = (items + warps_per_block - 1) / warps_per_block;
     const int64_t fill_blocks = (fill + moedc::kDispatchThreads - 1) / moedc::kDispatchThreads;
     if (blocks < fill_blocks) blocks = fill_blocks;
-    const int64_t max_blocks = (int64_t)sm_count() * 8;   // 8 x 256 threads fill an SM
-    if (blocks > max_blocks) blocks = max_blocks;
+    const void* fn = out_dtype == MOEDC_FP8_E4M3 ? (const void*)moedc::dispatch_kernel<true>
+                                                 : (const void*)moedc::dispatch_kernel<false>;
+    const int64_t resident = resident_blocks(fn, moedc::kDispatchThreads, 0);
+    if (blocks > resident) blocks = resident;
     if (blocks < 1) blocks = 1;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (out_dtype == MOEDC_FP8_E4M3)

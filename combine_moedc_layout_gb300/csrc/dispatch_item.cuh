@@ -14,59 +14,109 @@ namespace moedc {
 
 constexpr int kSlice = 512;   // channels per warp item
 
-// Lane `lane` of a warp holds entry k == lane of the token (k < K): its expert
-// id and slot.  Broadcast helpers read them back by k.
-struct Dest {
-    int e;
-    int s;
-};
+#ifndef MOEDC_DISPATCH_FASTDIV
+#define MOEDC_DISPATCH_FASTDIV 1
+#endif
 
+// binary32 value whose magnitude bit pattern is moved by d (clamped at zero),
+// keeping the sign
+__device__ __forceinline__ float nudge(float q, int d)
+{
+    const uint32_t b = __float_as_uint(q);
+    const uint32_t m = b & 0x7fffffffu;
+    const uint32_t n = d < 0 ? (m > (uint32_t)(-d) ? m - (uint32_t)(-d) : 0u) : m + (uint32_t)d;
+    return __uint_as_float((b & 0x80000000u) | n);
+}
+
+// e4m3 codes (low byte = first) of RN(a / s) and RN(b / s), where RN(./.) is
+// the correctly rounded binary32 quotient.
+//
+// With r = RN(1/s), q = RN(a * r) = (a/s)(1 + d1)(1 + d2) with |d1|, |d2| <=
+// 2^-24, so |q - a/s| < 2 ulp(a/s) and |q - RN(a/s)| < 2.5 ulp(a/s): at most 2
+// binary32 steps apart inside one binade, at most 5 when q falls into the
+// binade below (half-size steps); the subnormal range stays within 2 steps.
+// The satfinite nearest-even encoding is monotonic, so when the patterns 8
+// steps below and above q encode alike, every value between them - RN(a/s)
+// included - has that code and the division is not needed.  Otherwise (q sits
+// near an e4m3 rounding boundary) both quotients are computed exactly.
+__device__ __forceinline__ uint32_t quant_pair(float a, float b, float s, float r)
+{
+#if MOEDC_DISPATCH_FASTDIV
+    const float qa = __fmul_rn(a, r);
+    const float qb = __fmul_rn(b, r);
+    const uint32_t lo = pack_e4m3x2(nudge(qa, -8), nudge(qb, -8));
+    const uint32_t hi = pack_e4m3x2(nudge(qa, 8), nudge(qb, 8));
+    if (lo == hi) return lo;
+#endif
+    return pack_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+
+// Lane k < K of a warp holds entry k of the token (expert id and slot); the
+// store loops broadcast them by k.
 __device__ __forceinline__ bool dest_ok(int e, int s, int E, int cap)
 {
     return e >= 0 && e < E && s >= 0 && s < cap;
 }
 
+// The x data one lane needs for a work item (two 16-byte vectors).
+struct SliceX {
+    uint4 a, b;
+};
+
 // bf16: lane covers channels {slice*512 + j*256 + lane*8 .. +8}, j = 0, 1, so
 // each 16-byte access of the warp covers 512 contiguous bytes.
-__device__ __forceinline__ void dispatch_slice_bf16(const uint16_t* __restrict__ xrow, int H,
-                                                    int slice, int lane, int K, int my_e,
-                                                    int my_s, int E, int cap,
-                                                    uint16_t* __restrict__ recv)
+__device__ __forceinline__ SliceX load_slice_bf16(const uint16_t* __restrict__ xrow, int H,
+                                                  int slice, int lane)
+{
+    const int c0 = slice * kSlice + lane * 8;
+    const int c1 = c0 + 256;
+    SliceX v{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (c0 < H) v.a = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c0));
+    if (c1 < H) v.b = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c1));
+    return v;
+}
+
+__device__ __forceinline__ void store_slice_bf16(const SliceX& v, int H, int slice, int lane,
+                                                 int K, int my_e, int my_s, int E, int cap,
+                                                 uint16_t* __restrict__ recv)
 {
     const int c0 = slice * kSlice + lane * 8;
     const int c1 = c0 + 256;
     const bool a0 = c0 < H, a1 = c1 < H;
-    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-    if (a0) v0 = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c0));
-    if (a1) v1 = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c1));
     for (int k = 0; k < K; ++k) {
         const int e = __shfl_sync(0xffffffffu, my_e, k);
         const int s = __shfl_sync(0xffffffffu, my_s, k);
         if (!dest_ok(e, s, E, cap)) continue;
         uint16_t* row = recv + ((int64_t)e * cap + s) * H;
-        if (a0) st_global_cs(reinterpret_cast<uint4*>(row + c0), v0);
-        if (a1) st_global_cs(reinterpret_cast<uint4*>(row + c1), v1);
+        if (a0) st_global_cs(reinterpret_cast<uint4*>(row + c0), v.a);
+        if (a1) st_global_cs(reinterpret_cast<uint4*>(row + c1), v.b);
     }
 }
 
 // e4m3: lane covers 16 consecutive channels slice*512 + lane*16 .. +16, so
 // each 128-channel scale group is held by 8 adjacent lanes and one 16-byte
 // store per lane writes the lane's codes.
-__device__ __forceinline__ void dispatch_slice_fp8(const uint16_t* __restrict__ xrow, int H,
-                                                   int slice, int lane, int K, int my_e,
-                                                   int my_s, int E, int cap,
-                                                   uint8_t* __restrict__ recv,
-                                                   float* __restrict__ scales)
+__device__ __forceinline__ SliceX load_slice_fp8(const uint16_t* __restrict__ xrow, int H,
+                                                 int slice, int lane)
+{
+    const int c0 = slice * kSlice + lane * 16;
+    SliceX v{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (c0 < H) {   // H % 128 == 0: a scale group is all in or all out
+        v.a = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c0));
+        v.b = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c0 + 8));
+    }
+    return v;
+}
+
+__device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slice, int lane,
+                                                int K, int my_e, int my_s, int E, int cap,
+                                                uint8_t* __restrict__ recv,
+                                                float* __restrict__ scales)
 {
     const int G = H / 128;
     const int c0 = slice * kSlice + lane * 16;
-    const bool act = c0 < H;   // H % 128 == 0: a scale group is all in or all out
-    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-    if (act) {
-        a = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c0));
-        b = ld_global_nc(reinterpret_cast<const uint4*>(xrow + c0 + 8));
-    }
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const bool act = c0 < H;
+    const uint32_t w[8] = {v.a.x, v.a.y, v.a.z, v.a.w, v.b.x, v.b.y, v.b.z, v.b.w};
     float f[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -82,11 +132,12 @@ __device__ __forceinline__ void dispatch_slice_fp8(const uint16_t* __restrict__ 
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     amax = fmaxf(amax, 1e-4f);
     const float sc = __fdiv_rn(amax, 448.0f);
+    const float rc = __frcp_rn(sc);
     uint32_t p[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * j + 0], sc), __fdiv_rn(f[4 * j + 1], sc));
-        const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * j + 2], sc), __fdiv_rn(f[4 * j + 3], sc));
+        const uint32_t lo = quant_pair(f[4 * j + 0], f[4 * j + 1], sc, rc);
+        const uint32_t hi = quant_pair(f[4 * j + 2], f[4 * j + 3], sc, rc);
         p[j] = lo | (hi << 16);
     }
     const uint4 q = make_uint4(p[0], p[1], p[2], p[3]);
@@ -100,6 +151,25 @@ __device__ __forceinline__ void dispatch_slice_fp8(const uint16_t* __restrict__ 
         st_global_cs(reinterpret_cast<uint4*>(recv + row * H + c0), q);
         if (leader) st_global_cs_f32(scales + row * G + g, sc);
     }
+}
+
+template <bool kFp8>
+__device__ __forceinline__ SliceX load_slice(const uint16_t* xrow, int H, int slice, int lane)
+{
+    return kFp8 ? load_slice_fp8(xrow, H, slice, lane) : load_slice_bf16(xrow, H, slice, lane);
+}
+
+template <bool kFp8>
+__device__ __forceinline__ void store_slice(const SliceX& v, int H, int slice, int lane, int K,
+                                            int my_e, int my_s, int E, int cap, void* recv,
+                                            float* scales)
+{
+    if (kFp8)
+        store_slice_fp8(v, H, slice, lane, K, my_e, my_s, E, cap, static_cast<uint8_t*>(recv),
+                        scales);
+    else
+        store_slice_bf16(v, H, slice, lane, K, my_e, my_s, E, cap,
+                         static_cast<uint16_t*>(recv));
 }
 
 }  // namespace moedc

@@ -115,13 +115,8 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
             my_s = s_slot[t * K + lane];
             if (sl == 0 && dest_ok(my_e, my_s, E, cap)) src_idx[(int64_t)my_e * cap + my_s] = t;
         }
-        const uint16_t* xrow = x + (int64_t)t * H;
-        if (kFp8)
-            dispatch_slice_fp8(xrow, H, sl, lane, K, my_e, my_s, E, cap,
-                               static_cast<uint8_t*>(recv), scales);
-        else
-            dispatch_slice_bf16(xrow, H, sl, lane, K, my_e, my_s, E, cap,
-                                static_cast<uint16_t*>(recv));
+        const SliceX v = load_slice<kFp8>(x + (int64_t)t * H, H, sl, lane);
+        store_slice<kFp8>(v, H, sl, lane, K, my_e, my_s, E, cap, recv, scales);
     }
 }
 
@@ -168,8 +163,11 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     int64_t blocks = (items + moedc::kFusedWarps - 1) / moedc::kFusedWarps;
     const int64_t fill_blocks = ((int64_t)E * cap + moedc::kFusedThreads - 1) / moedc::kFusedThreads;
     if (blocks < fill_blocks) blocks = fill_blocks;
-    const int64_t max_blocks = (int64_t)sm_count() * 4;
-    if (blocks > max_blocks) blocks = max_blocks;
+    const void* fn = out_dtype == MOEDC_FP8_E4M3
+                         ? (const void*)moedc::fused_layout_dispatch_kernel<true>
+                         : (const void*)moedc::fused_layout_dispatch_kernel<false>;
+    const int64_t resident = resident_blocks(fn, moedc::kFusedThreads, (size_t)(2 * n + E) * 4);
+    if (blocks > resident) blocks = resident;
     if (blocks < 1) blocks = 1;
     const size_t sm = (size_t)(2 * n + E) * sizeof(int32_t);
     const uint16_t* xb = static_cast<const uint16_t*>(x);

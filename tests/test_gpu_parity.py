@@ -294,3 +294,44 @@ def test_runs_on_a_side_stream():
     s.synchronize()
     ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
     compare_layout(lay, ref_lay, c.T)
+
+
+def _boundary_case():
+    """e4m3 dispatch inputs whose quotients x/s land on or next to e4m3
+    rounding midpoints, where a shortcut through a reciprocal would be most
+    likely to round differently from the exact division."""
+    rng = np.random.default_rng(77)
+    T, H, K, E, R = 96, 1024, 2, 4, 2
+    codes = np.arange(0, 0x7E, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = (vals[:-1] + vals[1:]) / 2
+    x = np.empty((T, H), np.float32)
+    for t in range(T):
+        for g in range(H // 128):
+            if t % 3 == 0:
+                amax = 448.0                                   # s = 1: x/s = x exactly
+            else:
+                amax = float(np.exp(rng.uniform(-6, 6)))
+            m = rng.choice(mids, 128) * rng.choice([-1.0, 1.0], 128)
+            grp = (m * (amax / 448.0)).astype(np.float32)
+            grp[0] = amax
+            x[t, g * 128:(g + 1) * 128] = grp
+    c = synth.make_random_case(78, T=T, H=H, K=K, E=E, R=R, cap=None, dtype=synth.FP8_E4M3)
+    xb = synth.f32_to_bf16_bits(x)
+    # nudge every other value by one bf16 step to sit just beside the midpoint
+    step = np.where(rng.random(xb.shape) < 0.5, 0, rng.choice([-1, 1], xb.shape)).astype(np.int32)
+    xb = (xb.astype(np.int32) + step).astype(np.uint16)
+    xb[:, ::128] = synth.f32_to_bf16_bits(x[:, ::128])           # keep the amax entries
+    c.x = xb
+    return c
+
+
+def test_fp8_quotients_at_rounding_midpoints():
+    c = _boundary_case()
+    d = DevCase(c)
+    lay = run_layout(d)
+    recv, scales, src_idx = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, c.dtype)
+    torch.cuda.synchronize()
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap, fp8=True)
+    compare_dispatch(c, recv, scales, src_idx, ref_lay, ref_d)
