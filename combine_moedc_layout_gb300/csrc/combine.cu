@@ -6,6 +6,8 @@
 // a handful of tokens still spreads over the whole grid) and the zero-copy
 // combine input note (the caller's expert outputs are read in place, never
 // staged).  The kernel is an HBM read stream: K gathered rows per token.
+#include <climits>
+
 #include "common.cuh"
 
 // Tuning knobs (compile-time): 16-byte vectors per lane per gathered row,
@@ -137,6 +139,7 @@ extern "C" int moedc_combine(const void* expert_out, int E, int cap, int H,
         cap < 1)
         return MOEDC_ERR_ARG;
     if (!expert_out || !dev_status) return MOEDC_ERR_ARG;
+    if ((int64_t)E * cap > INT32_MAX) return MOEDC_ERR_ARG;
     if (T > 0 && (!topk_idx || !slot || !topk_weights || !y)) return MOEDC_ERR_ARG;
     if (!aligned(expert_out, 16) || !aligned(y, 16) || !aligned(topk_idx, 4) ||
         !aligned(slot, 4) || !aligned(topk_weights, 4) || !aligned(dev_status, 4))
@@ -149,6 +152,7 @@ extern "C" int moedc_combine(const void* expert_out, int E, int cap, int H,
     const int64_t resident =
         resident_blocks((const void*)moedc::combine_kernel, moedc::kCombineThreads, 0);
     if (blocks > resident) blocks = resident;
+    clear_stale_error();
     moedc::combine_kernel<<<(int)blocks, moedc::kCombineThreads, 0, stream>>>(
         static_cast<const uint16_t*>(expert_out), E, cap, H, topk_idx, slot, topk_weights, T, K,
         static_cast<uint16_t*>(y), dev_status);

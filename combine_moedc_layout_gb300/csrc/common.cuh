@@ -76,6 +76,11 @@ int sm_count();                 // multiprocessors of the current device
 // blocks of `kernel` resident on the whole current device at once
 int resident_blocks(const void* kernel, int threads, size_t smem);
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+// Launch checks read this library's own runtime error state (cudart is linked
+// statically, so it is not shared with other runtimes in the process).
+// clear_stale_error() drops a non-sticky error left by an earlier query so
+// that launch_status() reports only the launch that follows it.
+inline void clear_stale_error() { (void)cudaGetLastError(); }
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? MOEDC_OK : MOEDC_ERR_CUDA; }
 
 // Layout geometry: tokens per thread block of the layout kernels.

@@ -7,6 +7,8 @@
 // latency on MI300X + CX7" (flat stride over work items instead of per-block
 // token ranges).  On one GPU the "remote store" is a plain HBM store, so the
 // kernel is a write stream: each token row is read once and written K times.
+#include <climits>
+
 #include "dispatch_item.cuh"
 
 namespace moedc {
@@ -27,43 +29,41 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
 {
     const int lane = threadIdx.x % kWarp;
     const int nslice = (H + kSlice - 1) / kSlice;
-    const int64_t items = (int64_t)T * nslice;
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / kWarp);
+    const int nwarps = gridDim.x * (blockDim.x / kWarp);
+    const int dt = nwarps / nslice, dsl = nwarps - dt * nslice;
     bool bad = false;
 
-    // a work item's inputs: routing entry k == lane, and the lane's x vectors
-    auto load_item = [&](int64_t it, int& e, int& s, SliceX& v) {
-        e = -1;
-        s = -1;
+    // a work item's inputs: the destination row of routing entry k == lane,
+    // and the lane's x vectors
+    auto load_item = [&](const ItemCursor& c, int& row, SliceX& v) {
+        row = -1;
         v = SliceX{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (it >= items) return;
-        const int64_t t = it / nslice;
-        const int sl = (int)(it - t * nslice);
+        if (c.t >= T) return;
         if (lane < K) {
-            e = __ldg(topk_idx + t * K + lane);
-            s = __ldg(slot + t * K + lane);
+            const int e = __ldg(topk_idx + (int64_t)c.t * K + lane);
+            const int s = __ldg(slot + (int64_t)c.t * K + lane);
+            row = dest_row(e, s, E, cap);
+            if (c.sl == 0 && (e < -1 || e >= E)) bad = true;
         }
-        v = load_slice<kFp8>(x + t * H, H, sl, lane);
+        v = load_slice<kFp8>(x + (int64_t)c.t * H, H, c.sl, lane);
     };
-    int64_t item = (int64_t)blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
-    int my_e, my_s;
-    SliceX cur;
-    load_item(item, my_e, my_s, cur);
-    for (; item < items; item += nwarps) {
-        const int t = (int)(item / nslice);
-        const int sl = (int)(item - (int64_t)t * nslice);
+    ItemCursor cur;
+    cur.init(blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp, nslice);
+    int my_row;
+    SliceX xv;
+    load_item(cur, my_row, xv);
+    while (cur.t < T) {
         // the next item's routing and x travel while this one is stored
-        int nx_e, nx_s;
-        SliceX nxt;
-        load_item(item + nwarps, nx_e, nx_s, nxt);
-        if (sl == 0 && lane < K) {
-            if (my_e < -1 || my_e >= E) bad = true;
-            if (dest_ok(my_e, my_s, E, cap)) src_idx[(int64_t)my_e * cap + my_s] = t;
-        }
-        store_slice<kFp8>(cur, H, sl, lane, K, my_e, my_s, E, cap, recv, scales);
-        my_e = nx_e;
-        my_s = nx_s;
+        ItemCursor nxt = cur;
+        nxt.advance(dt, dsl, nslice);
+        int nx_row;
+        SliceX nx_v;
+        load_item(nxt, nx_row, nx_v);
+        if (cur.sl == 0 && lane < K && my_row >= 0) src_idx[my_row] = cur.t;
+        store_slice<kFp8>(xv, H, cur.sl, lane, K, my_row, recv, scales);
         cur = nxt;
+        my_row = nx_row;
+        xv = nx_v;
     }
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
 
@@ -91,6 +91,8 @@ static bool dispatch_args_ok(const void* x, int T, int H, const int32_t* topk_id
     if (out_dtype != MOEDC_BF16 && out_dtype != MOEDC_FP8_E4M3) return false;
     if (out_dtype == MOEDC_BF16 && H % 8 != 0) return false;
     if (out_dtype == MOEDC_FP8_E4M3 && H % 128 != 0) return false;
+    if ((int64_t)E * cap > INT32_MAX) return false;
+    if ((int64_t)T * ((H + 511) / 512) > INT32_MAX / 2) return false;
     if (!cnt || !recv || !src_idx || !dev_status) return false;
     if (out_dtype == MOEDC_FP8_E4M3 && !scales) return false;
     if (T > 0 && (!x || !topk_idx || !slot)) return false;
@@ -118,6 +120,7 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
     if (blocks > resident) blocks = resident;
     if (blocks < 1) blocks = 1;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
+    clear_stale_error();
     if (out_dtype == MOEDC_FP8_E4M3)
         moedc::dispatch_kernel<true><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
             xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,

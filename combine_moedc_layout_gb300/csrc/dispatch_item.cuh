@@ -14,40 +14,12 @@ namespace moedc {
 
 constexpr int kSlice = 512;   // channels per warp item
 
-#ifndef MOEDC_DISPATCH_FASTDIV
-#define MOEDC_DISPATCH_FASTDIV 1
-#endif
-
-// binary32 value whose magnitude bit pattern is moved by d (clamped at zero),
-// keeping the sign
-__device__ __forceinline__ float nudge(float q, int d)
+// e4m3 codes (low byte = first) of RN(a / s) and RN(b / s): one correctly
+// rounded binary32 division per element, then the satfinite nearest-even
+// encode.  (Multiplying by a rounded reciprocal instead was measured to save
+// no time here, so the division is kept as the definition states it.)
+__device__ __forceinline__ uint32_t quant_pair(float a, float b, float s)
 {
-    const uint32_t b = __float_as_uint(q);
-    const uint32_t m = b & 0x7fffffffu;
-    const uint32_t n = d < 0 ? (m > (uint32_t)(-d) ? m - (uint32_t)(-d) : 0u) : m + (uint32_t)d;
-    return __uint_as_float((b & 0x80000000u) | n);
-}
-
-// e4m3 codes (low byte = first) of RN(a / s) and RN(b / s), where RN(./.) is
-// the correctly rounded binary32 quotient.
-//
-// With r = RN(1/s), q = RN(a * r) = (a/s)(1 + d1)(1 + d2) with |d1|, |d2| <=
-// 2^-24, so |q - a/s| < 2 ulp(a/s) and |q - RN(a/s)| < 2.5 ulp(a/s): at most 2
-// binary32 steps apart inside one binade, at most 5 when q falls into the
-// binade below (half-size steps); the subnormal range stays within 2 steps.
-// The satfinite nearest-even encoding is monotonic, so when the patterns 8
-// steps below and above q encode alike, every value between them - RN(a/s)
-// included - has that code and the division is not needed.  Otherwise (q sits
-// near an e4m3 rounding boundary) both quotients are computed exactly.
-__device__ __forceinline__ uint32_t quant_pair(float a, float b, float s, float r)
-{
-#if MOEDC_DISPATCH_FASTDIV
-    const float qa = __fmul_rn(a, r);
-    const float qb = __fmul_rn(b, r);
-    const uint32_t lo = pack_e4m3x2(nudge(qa, -8), nudge(qb, -8));
-    const uint32_t hi = pack_e4m3x2(nudge(qa, 8), nudge(qb, 8));
-    if (lo == hi) return lo;
-#endif
     return pack_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
 }
 
@@ -77,19 +49,17 @@ __device__ __forceinline__ SliceX load_slice_bf16(const uint16_t* __restrict__ x
 }
 
 __device__ __forceinline__ void store_slice_bf16(const SliceX& v, int H, int slice, int lane,
-                                                 int K, int my_e, int my_s, int E, int cap,
-                                                 uint16_t* __restrict__ recv)
+                                                 int K, int my_row, uint16_t* __restrict__ recv)
 {
     const int c0 = slice * kSlice + lane * 8;
     const int c1 = c0 + 256;
     const bool a0 = c0 < H, a1 = c1 < H;
     for (int k = 0; k < K; ++k) {
-        const int e = __shfl_sync(0xffffffffu, my_e, k);
-        const int s = __shfl_sync(0xffffffffu, my_s, k);
-        if (!dest_ok(e, s, E, cap)) continue;
-        uint16_t* row = recv + ((int64_t)e * cap + s) * H;
-        if (a0) st_global_cs(reinterpret_cast<uint4*>(row + c0), v.a);
-        if (a1) st_global_cs(reinterpret_cast<uint4*>(row + c1), v.b);
+        const int row = __shfl_sync(0xffffffffu, my_row, k);
+        if (row < 0) continue;
+        uint16_t* dst = recv + (int64_t)row * H;
+        if (a0) st_global_cs(reinterpret_cast<uint4*>(dst + c0), v.a);
+        if (a1) st_global_cs(reinterpret_cast<uint4*>(dst + c1), v.b);
     }
 }
 
@@ -109,8 +79,7 @@ __device__ __forceinline__ SliceX load_slice_fp8(const uint16_t* __restrict__ xr
 }
 
 __device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slice, int lane,
-                                                int K, int my_e, int my_s, int E, int cap,
-                                                uint8_t* __restrict__ recv,
+                                                int K, int my_row, uint8_t* __restrict__ recv,
                                                 float* __restrict__ scales)
 {
     const int G = H / 128;
@@ -132,24 +101,21 @@ __device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slic
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     amax = fmaxf(amax, 1e-4f);
     const float sc = __fdiv_rn(amax, 448.0f);
-    const float rc = __frcp_rn(sc);
     uint32_t p[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = quant_pair(f[4 * j + 0], f[4 * j + 1], sc, rc);
-        const uint32_t hi = quant_pair(f[4 * j + 2], f[4 * j + 3], sc, rc);
+        const uint32_t lo = quant_pair(f[4 * j + 0], f[4 * j + 1], sc);
+        const uint32_t hi = quant_pair(f[4 * j + 2], f[4 * j + 3], sc);
         p[j] = lo | (hi << 16);
     }
     const uint4 q = make_uint4(p[0], p[1], p[2], p[3]);
     const bool leader = (lane & 7) == 0;
     const int g = c0 / 128;
     for (int k = 0; k < K; ++k) {
-        const int e = __shfl_sync(0xffffffffu, my_e, k);
-        const int s = __shfl_sync(0xffffffffu, my_s, k);
-        if (!dest_ok(e, s, E, cap) || !act) continue;
-        const int64_t row = (int64_t)e * cap + s;
-        st_global_cs(reinterpret_cast<uint4*>(recv + row * H + c0), q);
-        if (leader) st_global_cs_f32(scales + row * G + g, sc);
+        const int row = __shfl_sync(0xffffffffu, my_row, k);
+        if (row < 0 || !act) continue;
+        st_global_cs(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), q);
+        if (leader) st_global_cs_f32(scales + (int64_t)row * G + g, sc);
     }
 }
 
@@ -161,15 +127,39 @@ __device__ __forceinline__ SliceX load_slice(const uint16_t* xrow, int H, int sl
 
 template <bool kFp8>
 __device__ __forceinline__ void store_slice(const SliceX& v, int H, int slice, int lane, int K,
-                                            int my_e, int my_s, int E, int cap, void* recv,
-                                            float* scales)
+                                            int my_row, void* recv, float* scales)
 {
     if (kFp8)
-        store_slice_fp8(v, H, slice, lane, K, my_e, my_s, E, cap, static_cast<uint8_t*>(recv),
-                        scales);
+        store_slice_fp8(v, H, slice, lane, K, my_row, static_cast<uint8_t*>(recv), scales);
     else
-        store_slice_bf16(v, H, slice, lane, K, my_e, my_s, E, cap,
-                         static_cast<uint16_t*>(recv));
+        store_slice_bf16(v, H, slice, lane, K, my_row, static_cast<uint16_t*>(recv));
 }
+
+// Destination row index e * cap + s of a routing entry, or -1 when the entry
+// is masked, out of range or dropped (the host checks E * cap fits in int).
+__device__ __forceinline__ int dest_row(int e, int s, int E, int cap)
+{
+    return dest_ok(e, s, E, cap) ? e * cap + s : -1;
+}
+
+// Cursor over the flat (token, slice) item space of a grid-strided warp,
+// advanced by a fixed stride without dividing.
+struct ItemCursor {
+    int t, sl;
+    __device__ __forceinline__ void init(int item, int nslice)
+    {
+        t = item / nslice;
+        sl = item - t * nslice;
+    }
+    __device__ __forceinline__ void advance(int dt, int dsl, int nslice)
+    {
+        t += dt;
+        sl += dsl;
+        if (sl >= nslice) {
+            sl -= nslice;
+            t += 1;
+        }
+    }
+};
 
 }  // namespace moedc

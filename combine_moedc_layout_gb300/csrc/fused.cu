@@ -8,6 +8,8 @@
 // barrier cost more than the copy it was meant to parallelise (relay note:
 // block-local barriers only).  So every block recomputes the tiny layout in
 // shared memory, block 0 alone publishes it, and all blocks copy slices.
+#include <climits>
+
 #include "dispatch_item.cuh"
 
 namespace moedc {
@@ -109,14 +111,13 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
     for (int item = blockIdx.x * kFusedWarps + warp; item < items; item += nwarps) {
         const int t = item / nslice;
         const int sl = item - t * nslice;
-        int my_e = -1, my_s = -1;
+        int my_row = -1;
         if (lane < K) {
-            my_e = s_idx[t * K + lane];
-            my_s = s_slot[t * K + lane];
-            if (sl == 0 && dest_ok(my_e, my_s, E, cap)) src_idx[(int64_t)my_e * cap + my_s] = t;
+            my_row = dest_row(s_idx[t * K + lane], s_slot[t * K + lane], E, cap);
+            if (sl == 0 && my_row >= 0) src_idx[my_row] = t;
         }
         const SliceX v = load_slice<kFp8>(x + (int64_t)t * H, H, sl, lane);
-        store_slice<kFp8>(v, H, sl, lane, K, my_e, my_s, E, cap, recv, scales);
+        store_slice<kFp8>(v, H, sl, lane, K, my_row, recv, scales);
     }
 }
 
@@ -137,6 +138,8 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
         (out_dtype != MOEDC_BF16 && out_dtype != MOEDC_FP8_E4M3))
         return MOEDC_ERR_ARG;
     if (!num_tokens_per_expert || !num_tokens_per_rank || !dev_status || !recv || !src_idx)
+        return MOEDC_ERR_ARG;
+    if ((int64_t)E * cap > INT32_MAX || (int64_t)T * ((H + 511) / 512) > INT32_MAX / 2)
         return MOEDC_ERR_ARG;
     if (out_dtype == MOEDC_FP8_E4M3 && !scales) return MOEDC_ERR_ARG;
     if (T > 0 && (!x || !topk_idx || !is_token_in_rank || !slot)) return MOEDC_ERR_ARG;
@@ -171,6 +174,7 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     if (blocks < 1) blocks = 1;
     const size_t sm = (size_t)(2 * n + E) * sizeof(int32_t);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
+    clear_stale_error();
     if (out_dtype == MOEDC_FP8_E4M3)
         moedc::fused_layout_dispatch_kernel<true><<<(int)blocks, moedc::kFusedThreads, sm, stream>>>(
             xb, topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,

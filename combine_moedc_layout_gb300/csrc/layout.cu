@@ -377,6 +377,7 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
     const LayoutGeom g = layout_geometry(T, K, E, R);
     if (g.sweep) {
         const bool vec_ok = aligned(topk_idx, 16);
+        clear_stale_error();
         moedc::layout_sweep_kernel<<<g.blocks, moedc::kSweepThreads, 0, stream>>>(
             topk_idx, T, K, E, R, cap, vec_ok, num_tokens_per_expert, num_tokens_per_rank,
             is_token_in_rank, slot, dev_status);
@@ -388,6 +389,7 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
         const size_t sm = moedc::count_smem(g.tpc, K, E, R);
         if (ensure_smem_attr((const void*)moedc::layout_count_kernel, sm) != MOEDC_OK)
             return MOEDC_ERR_CUDA;
+        clear_stale_error();
         moedc::layout_count_kernel<<<g.blocks, moedc::kLayoutThreads, sm, stream>>>(
             topk_idx, T, K, E, R, g.tpc, ws_hist, ws_rank, dev_status);
         if (launch_status() != MOEDC_OK) return MOEDC_ERR_CUDA;
@@ -395,6 +397,7 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
     const size_t sm = moedc::assign_smem(g.tpc, K, E, R);
     if (ensure_smem_attr((const void*)moedc::layout_assign_kernel, sm) != MOEDC_OK)
         return MOEDC_ERR_CUDA;
+    clear_stale_error();
     moedc::layout_assign_kernel<<<g.blocks, moedc::kLayoutThreads, sm, stream>>>(
         topk_idx, T, K, E, R, cap, g.tpc, ws_hist, ws_rank, num_tokens_per_expert,
         num_tokens_per_rank, is_token_in_rank, slot, dev_status);
