@@ -252,6 +252,144 @@ def whole_job_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
     return step_bytes * world / (ms_per_step * 1e-3) / 1e9
 
 
+def side_workloads(dev) -> dict:
+    """Latency of the small workloads and per-kernel numbers of the skewed one.
+
+    low4 / low8 / low16 and default_ll: one round = moedc_layout_dispatch (a
+    single launch up to 1024 (token, k) entries) + moedc_combine, reported as
+    device us per round (events, eager), device us per CUDA-graph replay of the
+    round, and host us to enqueue one round through the Python binding
+    (ctypes included).  These footprints stay in L2: they are latencies, not
+    HBM rates.  imbalanced: layout, bf16 dispatch and combine back to back, us
+    and algorithmic GB/s per kernel.
+    """
+    import torch
+
+    from combine_moedc_layout_gb300 import moedc, synth
+
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name in ("low4", "low8", "low16", "default_ll"):
+        c = synth.make_case(name)
+        T, H, K, E, R, cap = c.T, c.H, c.K, c.E, c.R, c.cap
+        x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+        idx = torch.from_numpy(c.topk_idx).to(dev)
+        w = torch.from_numpy(c.topk_weights).to(dev)
+        g_ = torch.Generator(device=dev).manual_seed(c.seed)
+        eo = torch.randn((E, cap, H), device=dev, generator=g_).to(torch.bfloat16)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        cnt = torch.empty(E, dtype=torch.int32, device=dev)
+        rk = torch.empty(R, dtype=torch.int32, device=dev)
+        inr = torch.empty((T, R), dtype=torch.uint8, device=dev)
+        sl = torch.empty((T, K), dtype=torch.int32, device=dev)
+        recv, scales, src = moedc.alloc_recv(E, cap, H, c.dtype, dev)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+        def rnd(s_):
+            r = moedc.moedc_layout_dispatch(x, idx, T, H, K, E, R, cap, c.dtype, cnt, rk, inr, sl,
+                                            recv, scales, src, None, 0, st, s_)
+            r |= moedc.moedc_combine(eo, E, cap, H, idx, sl, w, T, K, y, st, s_)
+            if r != 0:
+                raise RuntimeError(f"libmoedc returned {r}")
+
+        for _ in range(20):
+            rnd(stream)
+        torch.cuda.synchronize(dev)
+        reps = 200
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        host = []
+        for a, b in evs:
+            a.record(stream)
+            h0 = time.perf_counter()
+            rnd(stream)
+            host.append(time.perf_counter() - h0)
+            b.record(stream)
+            torch.cuda.synchronize(dev)     # one round at a time: latency, not throughput
+        dev_us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+        # the same round captured once in a CUDA graph and replayed
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            rnd(side)
+            with torch.cuda.graph(graph, stream=side):
+                rnd(side)
+        torch.cuda.synchronize(dev)
+        gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(reps)]
+        ghost = []
+        for a, b in gevs:
+            a.record(stream)
+            h0 = time.perf_counter()
+            graph.replay()
+            ghost.append(time.perf_counter() - h0)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+        g_us = sorted(a.elapsed_time(b) * 1e3 for a, b in gevs)
+        if int(st.item()) != 0:
+            raise RuntimeError(f"{name}: device status {int(st.item())}")
+        med = lambda v: v[len(v) // 2]
+        out[name] = {"T": T, "H": H, "K": K, "E": E, "R": R, "cap": cap,
+                     "round": "moedc_layout_dispatch (e4m3, one launch) + moedc_combine",
+                     "device_us_per_round_median": med(dev_us),
+                     "device_us_p10": dev_us[reps // 10], "device_us_p90": dev_us[9 * reps // 10],
+                     "graph_replay_device_us_median": med(g_us),
+                     "host_enqueue_us_median": med(sorted(host)) * 1e6,
+                     "graph_replay_host_us_median": med(sorted(ghost)) * 1e6}
+        del recv, scales, eo, graph
+
+    # skewed routing, bf16 dispatch
+    c = synth.make_case("imbalanced")
+    T, H, K, E, R, cap = c.T, c.H, c.K, c.E, c.R, c.cap
+    N = int(((c.topk_idx >= 0) & (c.topk_idx < E)).sum())
+    nb = algorithmic_bytes(T, H, K, E, R, cap, N, False)
+    x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(c.topk_idx).to(dev)
+    w = torch.from_numpy(c.topk_weights).to(dev)
+    g_ = torch.Generator(device=dev).manual_seed(1)
+    eo = torch.randn((E, cap, H), device=dev, generator=g_).to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    rk = torch.empty(R, dtype=torch.int32, device=dev)
+    inr = torch.empty((T, R), dtype=torch.uint8, device=dev)
+    sl = torch.empty((T, K), dtype=torch.int32, device=dev)
+    recv, scales, src = moedc.alloc_recv(E, cap, H, c.dtype, dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    wsb = moedc.moedc_layout_workspace_bytes(T, K, E, R)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    reps = 200
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for i in range(reps + 10):
+        ev = evs[i - 10] if i >= 10 else None
+        if ev:
+            ev[0].record(stream)
+        r = moedc.moedc_layout(idx, T, K, E, R, cap, cnt, rk, inr, sl, ws, wsb, st, stream)
+        if ev:
+            ev[1].record(stream)
+        r |= moedc.moedc_dispatch(x, T, H, idx, sl, cnt, K, E, cap, c.dtype, recv, scales, src,
+                                  st, stream)
+        if ev:
+            ev[2].record(stream)
+        r |= moedc.moedc_combine(eo, E, cap, H, idx, sl, w, T, K, y, st, stream)
+        if ev:
+            ev[3].record(stream)
+        if r != 0:
+            raise RuntimeError(f"libmoedc returned {r}")
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"imbalanced: device status {int(st.item())}")
+    res = {"T": T, "H": H, "K": K, "E": E, "R": R, "cap": cap, "N": N,
+           "rank0_load_ratio": c.extra["rank0_load_ratio"], "dispatch_dtype": "bf16"}
+    for j, k in enumerate(("layout", "dispatch", "combine")):
+        us = sorted(e[j].elapsed_time(e[j + 1]) * 1e3 for e in evs)
+        m = sum(us) / len(us)
+        res[k] = {"us_mean": m, "us_median": us[len(us) // 2], "algorithmic_bytes": nb[k],
+                  "gbs": nb[k] / (m * 1e-6) / 1e9, "frac_of_8tbs": nb[k] / (m * 1e-6) / 1e9 / 8000}
+    out["imbalanced"] = res
+    return out
+
+
 def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     import torch
 
@@ -405,6 +543,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
 
+    side = None if args.no_side else side_workloads(dev)
     if rank != 0:
         return
     cpu = None
@@ -432,6 +571,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                             "expert_out; moedc_layout, moedc_dispatch, moedc_combine; y and "
                             "counts back to pinned host"},
             "gpu_launches": launches_per_step * K_steps,
+            "workloads": side,
             "clocks": clocks, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
 
@@ -443,6 +583,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the low-token / 128-token / imbalanced side measurements")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -29,36 +29,65 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
 {
     extern __shared__ int32_t smem[];
     const int n = T * K;
-    int32_t* s_idx = smem;          // [n]
-    int32_t* s_slot = s_idx + n;    // [n]
-    int32_t* s_cnt = s_slot + n;    // [E]
+    int32_t* s_idx = smem;                      // [n]
+    int32_t* s_slot = s_idx + n;                // [n]
+    int32_t* s_wcnt = s_slot + n;               // [kFusedWarps][E] per-warp counts, then offsets
+    int32_t* s_cnt = s_wcnt + kFusedWarps * E;  // [E] totals, then block 0's [R] rank counts
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int epr = E / R;
 
-    for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+    for (int i = threadIdx.x; i < kFusedWarps * E; i += blockDim.x) s_wcnt[i] = 0;
     for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = topk_idx[i];
     __syncthreads();
 
-    // layout, one warp, 32 entries at a time in (t, k) order
-    if (warp == 0) {
-        const unsigned lt = lanemask_lt();
-        for (int i0 = 0; i0 < n; i0 += kWarp) {
-            const int i = i0 + lane;
-            const int e = i < n ? s_idx[i] : -1;
-            const bool v = e >= 0 && e < E;
-            const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1);
-            int s = -1;
-            if (v) s = s_cnt[e] + __popc(peers & lt);
-            __syncwarp();
-            if (v && (peers & lt) == 0) s_cnt[e] += __popc(peers);
-            __syncwarp();
-            if (i < n) s_slot[i] = s;
+    // layout: each warp takes a contiguous run of 32-entry tiles in (t, k)
+    // order, counts it per expert, the counts are scanned across warps, then
+    // each warp ranks equal experts inside its tiles with __match_any_sync
+    const int run = ((n + kFusedWarps * kWarp - 1) / (kFusedWarps * kWarp)) * kWarp;
+    const int wbeg = min(n, warp * run);
+    const int wend = min(n, wbeg + run);
+    int32_t* my = s_wcnt + warp * E;
+    const unsigned lt = lanemask_lt();
+    for (int i0 = wbeg; i0 < wend; i0 += kWarp) {
+        const int i = i0 + lane;
+        const int e = i < wend ? s_idx[i] : -1;
+        const bool v = e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1);
+        if (v && (peers & lt) == 0) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int acc = 0;
+#pragma unroll
+        for (int w = 0; w < kFusedWarps; ++w) {
+            const int c = s_wcnt[w * E + e];
+            s_wcnt[w * E + e] = acc;
+            acc += c;
         }
+        s_cnt[e] = acc;
+    }
+    __syncthreads();
+    for (int i0 = wbeg; i0 < wend; i0 += kWarp) {
+        const int i = i0 + lane;
+        const int e = i < wend ? s_idx[i] : -1;
+        const bool v = e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1);
+        int sv = -1;
+        if (v) sv = my[e] + __popc(peers & lt);
+        __syncwarp();
+        if (v && (peers & lt) == 0) my[e] += __popc(peers);
+        __syncwarp();
+        if (i < wend) s_slot[i] = sv;
     }
     __syncthreads();
 
     if (blockIdx.x == 0) {
+        // block 0 publishes the layout; rank membership is a range test per
+        // (token, rank) pair, spread over all threads, counted in shared memory
+        int32_t* s_rank = s_cnt + E;   // [R] (after the totals)
+        for (int r = threadIdx.x; r < R; r += blockDim.x) s_rank[r] = 0;
         bool bad = false;
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             slot[i] = s_slot[i];
@@ -70,28 +99,19 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
             num_tokens_per_expert[e] = s_cnt[e];
             if (s_cnt[e] > cap) raise_status(status, MOEDC_ERR_CAPACITY);
         }
+        __syncthreads();   // s_rank zeroed
         for (int b = threadIdx.x; b < T * R; b += blockDim.x) {
             const int t = b / R;
             const int r = b - t * R;
+            const unsigned lo = (unsigned)(r * epr);
             uint8_t flag = 0;
-            for (int k = 0; k < K; ++k) {
-                const int e = s_idx[t * K + k];
-                if (e >= 0 && e < E && e / epr == r) flag = 1;
-            }
+            for (int k = 0; k < K; ++k)
+                flag |= ((unsigned)s_idx[t * K + k] - lo < (unsigned)epr) ? 1 : 0;
             is_token_in_rank[b] = flag;
+            if (flag) atomicAdd(&s_rank[r], 1);
         }
-        for (int r = threadIdx.x; r < R; r += blockDim.x) {
-            int c = 0;
-            for (int t = 0; t < T; ++t) {
-                bool in = false;
-                for (int k = 0; k < K; ++k) {
-                    const int e = s_idx[t * K + k];
-                    if (e >= 0 && e < E && e / epr == r) in = true;
-                }
-                c += in ? 1 : 0;
-            }
-            num_tokens_per_rank[r] = c;
-        }
+        __syncthreads();
+        for (int r = threadIdx.x; r < R; r += blockDim.x) num_tokens_per_rank[r] = s_rank[r];
     }
 
     // src_idx: -1 past each expert's count (grid-strided), t for filled slots
@@ -169,10 +189,11 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     const void* fn = out_dtype == MOEDC_FP8_E4M3
                          ? (const void*)moedc::fused_layout_dispatch_kernel<true>
                          : (const void*)moedc::fused_layout_dispatch_kernel<false>;
-    const int64_t resident = resident_blocks(fn, moedc::kFusedThreads, (size_t)(2 * n + E) * 4);
+    const int64_t resident = resident_blocks(
+        fn, moedc::kFusedThreads, (size_t)(2 * n + (moedc::kFusedWarps + 1) * E + R) * 4);
     if (blocks > resident) blocks = resident;
     if (blocks < 1) blocks = 1;
-    const size_t sm = (size_t)(2 * n + E) * sizeof(int32_t);
+    const size_t sm = (size_t)(2 * n + (moedc::kFusedWarps + 1) * E + R) * sizeof(int32_t);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
     if (out_dtype == MOEDC_FP8_E4M3)
