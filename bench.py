@@ -255,13 +255,15 @@ def whole_job_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
 def side_workloads(dev) -> dict:
     """Latency of the small workloads and per-kernel numbers of the skewed one.
 
-    low4 / low8 / low16 and default_ll: one round = moedc_layout_dispatch (a
-    single launch up to 1024 (token, k) entries) + moedc_combine, reported as
-    device us per round (events, eager), device us per CUDA-graph replay of the
-    round, and host us to enqueue one round through the Python binding
-    (ctypes included).  These footprints stay in L2: they are latencies, not
-    HBM rates.  imbalanced: layout, bf16 dispatch and combine back to back, us
-    and algorithmic GB/s per kernel.
+    T = 4, 8, 16, 32, 64 (hidden 6144, top-8 of 128, 16 ranks) and the
+    128-token / 288-expert workload: one MoE round = moedc_layout_dispatch (a
+    single launch up to 1024 (token, k) entries, e4m3) -> moedc_dequant_e4m3
+    (the identity expert) -> moedc_combine, reported as device us per round
+    (events, eager, one round at a time), device us per CUDA-graph replay of
+    the round, and host us to enqueue one round through the Python binding
+    (ctypes included) or to launch the graph.  These footprints stay in L2:
+    they are latencies, not HBM rates.  imbalanced: layout, bf16 dispatch and
+    combine back to back, us and algorithmic GB/s per kernel.
     """
     import torch
 
@@ -269,14 +271,15 @@ def side_workloads(dev) -> dict:
 
     out = {}
     stream = torch.cuda.current_stream(dev)
-    for name in ("low4", "low8", "low16", "default_ll"):
-        c = synth.make_case(name)
+    small = [("low4", 4), ("low8", 8), ("low16", 16), ("low32", 32), ("low64", 64),
+             ("default_ll", None)]
+    for name, t_over in small:
+        c = synth.make_case("low16" if name.startswith("low") else name, T=t_over)
         T, H, K, E, R, cap = c.T, c.H, c.K, c.E, c.R, c.cap
         x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
         idx = torch.from_numpy(c.topk_idx).to(dev)
         w = torch.from_numpy(c.topk_weights).to(dev)
-        g_ = torch.Generator(device=dev).manual_seed(c.seed)
-        eo = torch.randn((E, cap, H), device=dev, generator=g_).to(torch.bfloat16)
+        eo = torch.zeros((E, cap, H), dtype=torch.bfloat16, device=dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         cnt = torch.empty(E, dtype=torch.int32, device=dev)
         rk = torch.empty(R, dtype=torch.int32, device=dev)
@@ -288,6 +291,7 @@ def side_workloads(dev) -> dict:
         def rnd(s_):
             r = moedc.moedc_layout_dispatch(x, idx, T, H, K, E, R, cap, c.dtype, cnt, rk, inr, sl,
                                             recv, scales, src, None, 0, st, s_)
+            r |= moedc.moedc_dequant_e4m3(recv, scales, cnt, E, cap, H, eo, s_)
             r |= moedc.moedc_combine(eo, E, cap, H, idx, sl, w, T, K, y, st, s_)
             if r != 0:
                 raise RuntimeError(f"libmoedc returned {r}")
@@ -331,7 +335,8 @@ def side_workloads(dev) -> dict:
             raise RuntimeError(f"{name}: device status {int(st.item())}")
         med = lambda v: v[len(v) // 2]
         out[name] = {"T": T, "H": H, "K": K, "E": E, "R": R, "cap": cap,
-                     "round": "moedc_layout_dispatch (e4m3, one launch) + moedc_combine",
+                     "round": "moedc_layout_dispatch (e4m3, one launch) -> moedc_dequant_e4m3 "
+                              "(identity expert) -> moedc_combine: 3 launches",
                      "device_us_per_round_median": med(dev_us),
                      "device_us_p10": dev_us[reps // 10], "device_us_p90": dev_us[9 * reps // 10],
                      "graph_replay_device_us_median": med(g_us),

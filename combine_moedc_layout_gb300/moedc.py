@@ -32,7 +32,7 @@ FP8_E4M3 = 1
 
 EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes",
             "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
-            "moedc_layout_static_scratch")
+            "moedc_layout_static_scratch", "moedc_dequant_e4m3")
 
 STATIC_SCRATCH_BYTES = 1 << 20   # MOEDC_STATIC_SCRATCH_BYTES
 
@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_layout_dispatch.restype = I
     lib.moedc_layout_static_scratch.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P]
     lib.moedc_layout_static_scratch.restype = I
+    lib.moedc_dequant_e4m3.argtypes = [P, P, P, I, I, I, P, P]
+    lib.moedc_dequant_e4m3.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -149,6 +151,11 @@ def moedc_layout_dispatch(x, topk_idx, T, H, K, E, R, cap, out_dtype, num_tokens
         _p(x), _p(topk_idx), T, H, K, E, R, cap, out_dtype, _p(num_tokens_per_expert),
         _p(num_tokens_per_rank), _p(is_token_in_rank), _p(slot), _p(recv), _p(scales),
         _p(src_idx), _p(workspace), workspace_bytes, _p(dev_status), _stream(stream))
+
+
+def moedc_dequant_e4m3(recv, scales, num_tokens_per_expert, E, cap, H, out, stream=None) -> int:
+    return load().moedc_dequant_e4m3(_p(recv), _p(scales), _p(num_tokens_per_expert), E, cap, H,
+                                     _p(out), _stream(stream))
 
 
 # ---------------------------------------------------------------- conveniences
@@ -255,3 +262,14 @@ def layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int, cap
                                  lay.is_token_in_rank, lay.slot, recv, scales, src_idx, workspace,
                                  wsb, lay.status), "moedc_layout_dispatch")
     return lay, recv, scales, src_idx
+
+
+def dequant_e4m3(recv: torch.Tensor, scales: torch.Tensor, num_tokens_per_expert: torch.Tensor,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 [E, cap, H] view of an e4m3 receive buffer (filled rows only)."""
+    E, cap, H = recv.shape
+    if out is None:
+        out = torch.zeros((E, cap, H), dtype=torch.bfloat16, device=recv.device)
+    _check(moedc_dequant_e4m3(recv, scales, num_tokens_per_expert, E, cap, H, out),
+           "moedc_dequant_e4m3")
+    return out

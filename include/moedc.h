@@ -193,6 +193,19 @@ MOEDC_EXPORT int moedc_combine(const void* expert_out, int E, int cap, int H,
                   void* y, int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * e4m3 receive rows back to bf16 (the dequantisation q * s that pairs with
+ * the e4m3 dispatch; used as the identity expert of a dispatch -> expert ->
+ * combine round).  For every expert e, filled slot s < min(count[e], cap)
+ * and channel h of group g = h / 128:
+ *   out[e][s][h] = bf16_rne( float(recv[e][s][h]) * scales[e][s][g] )
+ * with one binary32 multiply.  Rows past an expert's count are not written.
+ * recv and out must be 16-byte aligned; H % 128 == 0.  No data errors.
+ */
+MOEDC_EXPORT int moedc_dequant_e4m3(const void* recv, const float* scales,
+                 const int32_t* num_tokens_per_expert, int E, int cap, int H,
+                 void* out_bf16, cudaStream_t stream);
+
+/*
  * Layout followed by dispatch, with the outputs of both calls
  * [MORI614 notes on low token counts: host enqueue and idle warps dominate].
  * For T * K <= MOEDC_FUSED_MAX_ENTRIES this is ONE kernel launch: every

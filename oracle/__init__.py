@@ -62,6 +62,7 @@ def _load():
     lib.oracle_e4m3_encode_n.argtypes = [P, P, I64]
     lib.oracle_e4m3_decode_n.argtypes = [P, P, I64]
     lib.oracle_f32_to_bf16_n.argtypes = [P, P, I64]
+    lib.oracle_dequant_e4m3.argtypes = [P, P, P, I, I, I, P]
     _lib = lib
     return lib
 
@@ -145,3 +146,18 @@ def combine(expert_out: np.ndarray, topk_idx: np.ndarray, slot: np.ndarray,
     status = _load().oracle_combine(_ptr(expert_out), E, cap, H, _ptr(topk_idx), _ptr(slot),
                                     _ptr(topk_weights), T, K, _ptr(y))
     return dict(y=y, status=status)
+
+
+def dequant_e4m3(recv: np.ndarray, scales: np.ndarray, num_tokens_per_expert: np.ndarray,
+                 out: np.ndarray | None = None) -> np.ndarray:
+    """recv uint8 [E, cap, H], scales float32 [E, cap, H/128] -> bf16 bits
+    [E, cap, H]; rows past each expert's count keep `out`'s contents (zeros
+    by default)."""
+    recv = np.ascontiguousarray(recv, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    cnt = np.ascontiguousarray(num_tokens_per_expert, dtype=np.int32)
+    E, cap, H = recv.shape
+    if out is None:
+        out = np.zeros((E, cap, H), np.uint16)
+    _load().oracle_dequant_e4m3(_ptr(recv), _ptr(scales), _ptr(cnt), E, cap, H, _ptr(out))
+    return out

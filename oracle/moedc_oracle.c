@@ -303,3 +303,30 @@ int oracle_combine(const uint16_t* expert_out, int E, int cap, int H,
     }
     return status;
 }
+
+/* ------------------------------------------------------------- dequant */
+/*
+ * e4m3 receive rows back to bf16 (the "identity expert" of a dispatch ->
+ * expert -> combine round): for every expert e and filled slot
+ * s < min(num_tokens_per_expert[e], cap), channel h of group g = h / 128:
+ *   p = decode(recv[e][s][h]) * scales[e][s][g]     (binary32 multiply)
+ *   out[e][s][h] = bf16(p), nearest even.
+ * Rows past an expert's count are left untouched.
+ */
+void oracle_dequant_e4m3(const uint8_t* recv, const float* scales,
+                         const int32_t* num_tokens_per_expert, int E, int cap, int H,
+                         uint16_t* out)
+{
+    int G = H / 128;
+    for (int e = 0; e < E; ++e) {
+        int filled = num_tokens_per_expert[e] < cap ? num_tokens_per_expert[e] : cap;
+        for (int s = 0; s < filled; ++s) {
+            int64_t row = (int64_t)e * cap + s;
+            for (int h = 0; h < H; ++h) {
+                float v = oracle_e4m3_decode(recv[row * H + h]);
+                float p = v * scales[row * G + h / 128];
+                out[row * H + h] = oracle_f32_to_bf16(p);
+            }
+        }
+    }
+}

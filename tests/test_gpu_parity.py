@@ -335,3 +335,48 @@ def test_fp8_quotients_at_rounding_midpoints():
     ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
     ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap, fp8=True)
     compare_dispatch(c, recv, scales, src_idx, ref_lay, ref_d)
+
+
+@pytest.mark.parametrize("key", ["low16", "default_ll", "throughput", "r:multiblock_fp8",
+                                 "r:huge_values", "r:tiny_values", "r:k32_e1024"])
+def test_dequant_parity(key):
+    c = get_case(key)
+    d = DevCase(c)
+    lay = run_layout(d)
+    recv, scales, src_idx = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, c.dtype)
+    out = moedc.dequant_e4m3(recv, scales, lay.num_tokens_per_expert)
+    torch.cuda.synchronize()
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap, fp8=True)
+    ref = oracle.dequant_e4m3(ref_d["recv"], ref_d["scales"], ref_lay["num_tokens_per_expert"])
+    from parity_util import valid_rows
+    rows = valid_rows(ref_lay["num_tokens_per_expert"], c.cap)
+    got = bits_host(out.reshape(c.E * c.cap, c.H).index_select(0, torch.from_numpy(rows).cuda()))
+    np.testing.assert_array_equal(got, ref.reshape(c.E * c.cap, c.H)[rows])
+
+
+@pytest.mark.parametrize("T", [4, 16, 64])
+def test_moe_round_with_identity_expert(T):
+    """Fused layout + e4m3 dispatch -> dequant (identity expert) -> combine,
+    with weights renormalised over each token's entries: y matches the oracle
+    chain bit for bit and stays within the e4m3 error of x."""
+    c = synth.make_case("low16", T=T)
+    w = c.topk_weights / c.topk_weights.sum(axis=1, keepdims=True, dtype=np.float32)
+    c.topk_weights = np.ascontiguousarray(w.astype(np.float32))
+    d = DevCase(c)
+    lay, recv, scales, src_idx = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, c.dtype)
+    eo = moedc.dequant_e4m3(recv, scales, lay.num_tokens_per_expert)
+    y = moedc.combine(eo, d.topk_idx, lay.slot, d.topk_weights, status=lay.status)
+    torch.cuda.synchronize()
+    assert int(lay.status.item()) == 0
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap, fp8=True)
+    ref_eo = oracle.dequant_e4m3(ref_d["recv"], ref_d["scales"], ref_lay["num_tokens_per_expert"])
+    ref_y = oracle.combine(ref_eo, c.topk_idx, ref_lay["slot"], c.topk_weights)["y"]
+    compare_combine(y, ref_y)
+    x = oracle.bf16_to_f32(c.x).astype(np.float64)
+    yy = oracle.bf16_to_f32(bits_host(y)).astype(np.float64)
+    amax = np.abs(x).reshape(T, -1, 128).max(axis=2).repeat(128, axis=1)
+    # e4m3 relative step is 2^-3 (half of it per rounding) of the group scale
+    # range, plus the bf16 roundings of the dequantised rows and of y
+    assert (np.abs(yy - x) <= amax * 2.0**-4 + np.abs(x) * 2.0**-6).all()

@@ -251,3 +251,47 @@ def test_fp8_quotient_is_one_rounded_division():
             assert (d["recv"][0, 0] != cm).any()
             found += 1
     assert found >= 3
+
+
+# --------------------------------------------------------------- dequant
+
+@pytest.mark.parametrize("code,scale,expect", [
+    (0x7E, 2.0, 896.0), (0xFE, 0.25, -112.0), (0x01, 1.0, 2.0**-9), (0x00, 3.0, 0.0),
+    (0x38, 1.5, 1.5), (0x3A, 0.5, 0.625),
+])
+def test_dequant_closed_forms(code, scale, expect):
+    r = np.full((1, 1, 128), code, np.uint8)
+    out = oracle.dequant_e4m3(r, np.array([[[scale]]], np.float32), np.array([1], np.int32))
+    assert _bf16(out[0, 0, :1])[0] == np.float32(expect)
+
+
+def test_dequant_matches_torch_decode_multiply_cast():
+    rng = np.random.default_rng(21)
+    E, cap, H = 3, 5, 256
+    codes = rng.integers(0, 256, (E, cap, H), dtype=np.int64).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x11                 # dispatch never writes NaN codes
+    sc = np.exp(rng.uniform(-20, 5, (E, cap, H // 128))).astype(np.float32)
+    cnt = np.array([5, 2, 0], np.int32)
+    got = oracle.dequant_e4m3(codes, sc, cnt)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).float()
+    ref = (dec * torch.from_numpy(np.repeat(sc, 128, axis=2))).to(torch.bfloat16)
+    ref = ref.view(torch.int16).numpy().view(np.uint16)
+    for e in range(E):
+        np.testing.assert_array_equal(got[e, :cnt[e]], ref[e, :cnt[e]])
+        assert (got[e, cnt[e]:] == 0).all()                # rows past the count untouched
+
+
+def test_dispatch_then_dequant_error_bound():
+    c = synth.make_case("low8")
+    lay = _run_layout(c)
+    d = oracle.dispatch(c.x, c.topk_idx, lay["slot"], c.E, c.cap, fp8=True)
+    deq = oracle.dequant_e4m3(d["recv"], d["scales"], lay["num_tokens_per_expert"])
+    x = _bf16(c.x).astype(np.float64)
+    for t in range(c.T):
+        for k in range(c.K):
+            e, s = c.topk_idx[t, k], lay["slot"][t, k]
+            y = _bf16(deq[e, s]).astype(np.float64)
+            sc = np.repeat(d["scales"][e, s].astype(np.float64), 128)
+            # e4m3 half-ulp of x/s times s, plus the bf16 rounding of the product
+            bound = 0.5 * _e4m3_ulp(x[t] / sc) * sc * (1 + 2.0**-20) + np.abs(y) * 2.0**-8
+            assert (np.abs(y - x[t]) <= bound).all()
