@@ -263,7 +263,9 @@ def side_workloads(dev) -> dict:
     the round, and host us to enqueue one round through the Python binding
     (ctypes included) or to launch the graph.  These footprints stay in L2:
     they are latencies, not HBM rates.  imbalanced: layout, bf16 dispatch and
-    combine back to back, us and algorithmic GB/s per kernel.
+    combine back to back, us and algorithmic GB/s per kernel.  rank_major: the
+    same 4096-token e4m3 workload through rank layout, rank dispatch and rank
+    combine (one row per token and destination rank).
     """
     import torch
 
@@ -392,6 +394,62 @@ def side_workloads(dev) -> dict:
         res[k] = {"us_mean": m, "us_median": us[len(us) // 2], "algorithmic_bytes": nb[k],
                   "gbs": nb[k] / (m * 1e-6) / 1e9, "frac_of_8tbs": nb[k] / (m * 1e-6) / 1e9 / 8000}
     out["imbalanced"] = res
+    del recv, scales, eo, src
+
+    # rank-major packed receive on the 4096-token e4m3 workload: one row per
+    # (token, destination rank) instead of one per (token, expert)
+    c = synth.make_case(WORKLOAD)
+    T, H, K, E, R, cap = c.T, c.H, c.K, c.E, c.R, c.cap
+    G = H // 128
+    x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(c.topk_idx).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    rk = torch.empty(R, dtype=torch.int32, device=dev)
+    inr = torch.empty((T, R), dtype=torch.uint8, device=dev)
+    sl = torch.empty((T, K), dtype=torch.int32, device=dev)
+    wsb = moedc.moedc_layout_workspace_bytes(T, K, E, R)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    assert moedc.moedc_layout(idx, T, K, E, R, cap, cnt, rk, inr, sl, ws, wsb, st, stream) == 0
+    torch.cuda.synchronize(dev)
+    rows = int(rk.sum().item())
+    cap_rank = int(rk.max().item())
+    rslot = torch.empty((T, R), dtype=torch.int32, device=dev)
+    rrecv, rscales, rsrc = moedc.alloc_recv(R, cap_rank, H, c.dtype, dev)
+    g_ = torch.Generator(device=dev).manual_seed(2)
+    rout = torch.randn((R, cap_rank, H), device=dev, generator=g_).to(torch.bfloat16)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    rb = {"rank_layout": T * R + 4 * T * R,
+          "rank_dispatch": 2 * H * T + rows * (H + 4 * G) + 4 * T * R + 4 * R * cap_rank,
+          "rank_combine": rows * 2 * H + 4 * T * R + 2 * T * H}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for i in range(reps + 10):
+        ev = evs[i - 10] if i >= 10 else None
+        if ev:
+            ev[0].record(stream)
+        r = moedc.moedc_rank_layout(inr, T, R, cap_rank, rslot, st, stream)
+        if ev:
+            ev[1].record(stream)
+        r |= moedc.moedc_rank_dispatch(x, T, H, rslot, rk, R, cap_rank, c.dtype, rrecv, rscales,
+                                       rsrc, stream)
+        if ev:
+            ev[2].record(stream)
+        r |= moedc.moedc_rank_combine(rout, R, cap_rank, H, rslot, T, y, stream)
+        if ev:
+            ev[3].record(stream)
+        if r != 0:
+            raise RuntimeError(f"libmoedc returned {r}")
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"rank-major: device status {int(st.item())}")
+    res = {"T": T, "H": H, "R": R, "cap_rank": cap_rank, "rows": rows,
+           "rows_expert_major": int(cnt.sum().item()), "dispatch_dtype": "e4m3"}
+    for j, k in enumerate(("rank_layout", "rank_dispatch", "rank_combine")):
+        us = sorted(e[j].elapsed_time(e[j + 1]) * 1e3 for e in evs)
+        m = sum(us) / len(us)
+        res[k] = {"us_mean": m, "us_median": us[len(us) // 2], "algorithmic_bytes": rb[k],
+                  "gbs": rb[k] / (m * 1e-6) / 1e9, "frac_of_8tbs": rb[k] / (m * 1e-6) / 1e9 / 8000}
+    out["rank_major"] = res
     return out
 
 

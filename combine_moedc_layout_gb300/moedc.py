@@ -32,7 +32,8 @@ FP8_E4M3 = 1
 
 EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes",
             "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
-            "moedc_layout_static_scratch", "moedc_dequant_e4m3")
+            "moedc_layout_static_scratch", "moedc_dequant_e4m3", "moedc_rank_layout",
+            "moedc_rank_dispatch", "moedc_rank_combine")
 
 STATIC_SCRATCH_BYTES = 1 << 20   # MOEDC_STATIC_SCRATCH_BYTES
 
@@ -79,6 +80,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_layout_static_scratch.restype = I
     lib.moedc_dequant_e4m3.argtypes = [P, P, P, I, I, I, P, P]
     lib.moedc_dequant_e4m3.restype = I
+    lib.moedc_rank_layout.argtypes = [P, I, I, I, P, P, P]
+    lib.moedc_rank_layout.restype = I
+    lib.moedc_rank_dispatch.argtypes = [P, I, I, P, P, I, I, I, P, P, P, P]
+    lib.moedc_rank_dispatch.restype = I
+    lib.moedc_rank_combine.argtypes = [P, I, I, I, P, I, P, P]
+    lib.moedc_rank_combine.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -156,6 +163,23 @@ def moedc_layout_dispatch(x, topk_idx, T, H, K, E, R, cap, out_dtype, num_tokens
 def moedc_dequant_e4m3(recv, scales, num_tokens_per_expert, E, cap, H, out, stream=None) -> int:
     return load().moedc_dequant_e4m3(_p(recv), _p(scales), _p(num_tokens_per_expert), E, cap, H,
                                      _p(out), _stream(stream))
+
+
+def moedc_rank_layout(is_token_in_rank, T, R, cap_rank, rank_slot, dev_status, stream=None) -> int:
+    return load().moedc_rank_layout(_p(is_token_in_rank), T, R, cap_rank, _p(rank_slot),
+                                    _p(dev_status), _stream(stream))
+
+
+def moedc_rank_dispatch(x, T, H, rank_slot, num_tokens_per_rank, R, cap_rank, out_dtype,
+                        recv_rank, scales_rank, rank_src_idx, stream=None) -> int:
+    return load().moedc_rank_dispatch(_p(x), T, H, _p(rank_slot), _p(num_tokens_per_rank), R,
+                                      cap_rank, out_dtype, _p(recv_rank), _p(scales_rank),
+                                      _p(rank_src_idx), _stream(stream))
+
+
+def moedc_rank_combine(rank_out, R, cap_rank, H, rank_slot, T, y, stream=None) -> int:
+    return load().moedc_rank_combine(_p(rank_out), R, cap_rank, H, _p(rank_slot), T, _p(y),
+                                     _stream(stream))
 
 
 # ---------------------------------------------------------------- conveniences
@@ -273,3 +297,33 @@ def dequant_e4m3(recv: torch.Tensor, scales: torch.Tensor, num_tokens_per_expert
     _check(moedc_dequant_e4m3(recv, scales, num_tokens_per_expert, E, cap, H, out),
            "moedc_dequant_e4m3")
     return out
+
+
+def rank_layout(lay: Layout, cap_rank: int) -> torch.Tensor:
+    """rank_slot [T, R] from a Layout (raises on argument errors)."""
+    T, R = lay.is_token_in_rank.shape
+    rank_slot = torch.empty((T, R), dtype=torch.int32, device=lay.slot.device)
+    _check(moedc_rank_layout(lay.is_token_in_rank, T, R, cap_rank, rank_slot, lay.status),
+           "moedc_rank_layout")
+    return rank_slot
+
+
+def rank_dispatch(x: torch.Tensor, rank_slot: torch.Tensor, lay: Layout, cap_rank: int,
+                  out_dtype: int):
+    """Returns (recv_rank [R, cap_rank, H], scales_rank or None, rank_src_idx [R, cap_rank])."""
+    _need(x, torch.bfloat16, "x")
+    T, H = x.shape
+    R = rank_slot.shape[1]
+    recv, scales, src = alloc_recv(R, cap_rank, H, out_dtype, x.device)
+    _check(moedc_rank_dispatch(x, T, H, rank_slot, lay.num_tokens_per_rank, R, cap_rank,
+                               out_dtype, recv, scales, src), "moedc_rank_dispatch")
+    return recv, scales, src
+
+
+def rank_combine(rank_out: torch.Tensor, rank_slot: torch.Tensor) -> torch.Tensor:
+    _need(rank_out, torch.bfloat16, "rank_out")
+    R, cap_rank, H = rank_out.shape
+    T = rank_slot.shape[0]
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=rank_out.device)
+    _check(moedc_rank_combine(rank_out, R, cap_rank, H, rank_slot, T, y), "moedc_rank_combine")
+    return y

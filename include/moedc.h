@@ -206,6 +206,42 @@ MOEDC_EXPORT int moedc_dequant_e4m3(const void* recv, const float* scales,
                  void* out_bf16, cudaStream_t stream);
 
 /*
+ * Rank-major packed receive [UCCL749 title: tokens batched per destination].
+ * A token goes to a rank once, however many of its experts live there, into
+ * that rank's contiguous buffer of cap_rank rows.
+ *
+ * moedc_rank_layout: for each rank r, in ascending token order,
+ *   rank_slot[t][r] = number of earlier tokens with is_token_in_rank[.][r] = 1,
+ *                     when is_token_in_rank[t][r] = 1; -1 otherwise.
+ *   Data error (dev_status): MOEDC_ERR_CAPACITY when a rank receives more than
+ *   cap_rank tokens (slots keep counting; rows at slot >= cap_rank are dropped).
+ *   is_token_in_rank and num_tokens_per_rank come from moedc_layout.
+ *
+ * moedc_rank_dispatch: for each (t, r) with j = rank_slot[t][r] in [0, cap_rank):
+ *   rank_src_idx[r][j] = t; recv_rank[r][j][:] = x[t][:] (MOEDC_BF16), or the
+ *   e4m3 codes and per-128 fp32 scales of x[t] by the moedc_dispatch rule
+ *   (MOEDC_FP8_E4M3, scales_rank [R, cap_rank, H/128]).  rank_src_idx = -1
+ *   for j in [num_tokens_per_rank[r], cap_rank); other rows are not written.
+ *
+ * moedc_rank_combine: each rank returns one bf16 partial row per received
+ *   token (rank_out [R, cap_rank, H], the weighted sum over the token's
+ *   experts on that rank, formed on the expert side), and
+ *     y[t][h] = bf16_rne( sum over r ascending of float(rank_out[r][j][h]) )
+ *   over the ranks with j = rank_slot[t][r] in [0, cap_rank), binary32
+ *   accumulator from +0.  A token in no rank gives +0.
+ * Arguments: T >= 0, 1 <= R <= MOEDC_MAX_E, cap_rank >= 1; H as for
+ * moedc_dispatch / moedc_combine; x, recv_rank, rank_out, y 16-byte aligned.
+ */
+MOEDC_EXPORT int moedc_rank_layout(const uint8_t* is_token_in_rank, int T, int R, int cap_rank,
+                 int32_t* rank_slot, int32_t* dev_status, cudaStream_t stream);
+MOEDC_EXPORT int moedc_rank_dispatch(const void* x, int T, int H, const int32_t* rank_slot,
+                 const int32_t* num_tokens_per_rank, int R, int cap_rank, int out_dtype,
+                 void* recv_rank, float* scales_rank, int32_t* rank_src_idx,
+                 cudaStream_t stream);
+MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, int H,
+                 const int32_t* rank_slot, int T, void* y, cudaStream_t stream);
+
+/*
  * Layout followed by dispatch, with the outputs of both calls
  * [MORI614 notes on low token counts: host enqueue and idle warps dominate].
  * For T * K <= MOEDC_FUSED_MAX_ENTRIES this is ONE kernel launch: every

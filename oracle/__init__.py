@@ -63,6 +63,10 @@ def _load():
     lib.oracle_e4m3_decode_n.argtypes = [P, P, I64]
     lib.oracle_f32_to_bf16_n.argtypes = [P, P, I64]
     lib.oracle_dequant_e4m3.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_rank_layout.argtypes = [P, I, I, I, P]
+    lib.oracle_rank_layout.restype = I
+    lib.oracle_rank_dispatch.argtypes = [P, I, I, P, I, I, I, P, P, P]
+    lib.oracle_rank_combine.argtypes = [P, I, I, I, P, I, P]
     _lib = lib
     return lib
 
@@ -161,3 +165,38 @@ def dequant_e4m3(recv: np.ndarray, scales: np.ndarray, num_tokens_per_expert: np
         out = np.zeros((E, cap, H), np.uint16)
     _load().oracle_dequant_e4m3(_ptr(recv), _ptr(scales), _ptr(cnt), E, cap, H, _ptr(out))
     return out
+
+
+def rank_layout(is_token_in_rank: np.ndarray, cap_rank: int) -> dict:
+    """rank_slot [T, R] (position of token t in rank r's buffer, -1 if absent) and status."""
+    inr = np.ascontiguousarray(is_token_in_rank, dtype=np.uint8)
+    T, R = inr.shape
+    slot = np.empty((T, R), np.int32)
+    status = _load().oracle_rank_layout(_ptr(inr), T, R, cap_rank, _ptr(slot))
+    return dict(rank_slot=slot, status=status)
+
+
+def rank_dispatch(x: np.ndarray, rank_slot: np.ndarray, cap_rank: int, fp8: bool) -> dict:
+    """recv_rank [R, cap_rank, H] (bf16 bits or e4m3 codes), scales_rank
+    [R, cap_rank, H/128] (e4m3 only), rank_src_idx [R, cap_rank]."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    rank_slot = np.ascontiguousarray(rank_slot, dtype=np.int32)
+    T, H = x.shape
+    R = rank_slot.shape[1]
+    recv = np.zeros((R, cap_rank, H), np.uint8 if fp8 else np.uint16)
+    scales = np.zeros((R, cap_rank, H // 128), np.float32) if fp8 else np.zeros(1, np.float32)
+    src = np.empty((R, cap_rank), np.int32)
+    _load().oracle_rank_dispatch(_ptr(x), T, H, _ptr(rank_slot), R, cap_rank, 1 if fp8 else 0,
+                                 _ptr(recv), _ptr(scales), _ptr(src))
+    return dict(recv_rank=recv, scales_rank=scales if fp8 else None, rank_src_idx=src)
+
+
+def rank_combine(rank_out: np.ndarray, rank_slot: np.ndarray) -> np.ndarray:
+    """rank_out bf16 bits [R, cap_rank, H] -> y bf16 bits [T, H]."""
+    rank_out = np.ascontiguousarray(rank_out, dtype=np.uint16)
+    rank_slot = np.ascontiguousarray(rank_slot, dtype=np.int32)
+    R, cap_rank, H = rank_out.shape
+    T = rank_slot.shape[0]
+    y = np.empty((T, H), np.uint16)
+    _load().oracle_rank_combine(_ptr(rank_out), R, cap_rank, H, _ptr(rank_slot), T, _ptr(y))
+    return y

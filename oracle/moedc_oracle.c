@@ -330,3 +330,109 @@ void oracle_dequant_e4m3(const uint8_t* recv, const float* scales,
         }
     }
 }
+
+/* ------------------------------------------------ rank-major packed receive */
+/*
+ * Batching tokens per destination rank (UCCL PR #749, "[EP] Low-latency mode
+ * batch tokens per destination"): a token goes to a rank once, however many
+ * of its experts live there.
+ *
+ * Rank layout: for each rank r, visiting tokens in ascending t,
+ *   rank_slot[t][r] = number of earlier tokens t' < t with
+ *                     is_token_in_rank[t'][r] = 1, when is_token_in_rank[t][r]
+ *                     is 1; -1 otherwise.
+ * Returns CAPACITY when some rank receives more than cap_rank tokens (the
+ * slots keep counting, rows at slot >= cap_rank are dropped downstream).
+ */
+int oracle_rank_layout(const uint8_t* is_token_in_rank, int T, int R, int cap_rank,
+                       int32_t* rank_slot)
+{
+    int status = ORACLE_OK;
+    for (int r = 0; r < R; ++r) {
+        int count = 0;
+        for (int t = 0; t < T; ++t) {
+            if (is_token_in_rank[(int64_t)t * R + r]) {
+                rank_slot[(int64_t)t * R + r] = count;
+                count += 1;
+            } else {
+                rank_slot[(int64_t)t * R + r] = -1;
+            }
+        }
+        if (count > cap_rank)
+            status = raise_status(status, ORACLE_ERR_CAPACITY);
+    }
+    return status;
+}
+
+/*
+ * Rank dispatch: rank_src_idx[R][cap_rank] starts at -1; for each (t, r) with
+ * slot j = rank_slot[t][r] in [0, cap_rank):
+ *   rank_src_idx[r][j] = t
+ *   bf16: recv_rank[r][j][:] = x[t][:]
+ *   e4m3: per group g of 128 channels the same rule as expert dispatch:
+ *         a = max |x|, a = fmaxf(a, 1e-4f), s = a / 448.0f, codes = e4m3(x / s),
+ *         scales_rank[r][j][g] = s.
+ */
+void oracle_rank_dispatch(const uint16_t* x, int T, int H, const int32_t* rank_slot, int R,
+                          int cap_rank, int fp8, void* recv_rank, float* scales_rank,
+                          int32_t* rank_src_idx)
+{
+    int G = H / 128;
+    for (int64_t i = 0; i < (int64_t)R * cap_rank; ++i)
+        rank_src_idx[i] = -1;
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* xr = x + (int64_t)t * H;
+        for (int r = 0; r < R; ++r) {
+            int j = rank_slot[(int64_t)t * R + r];
+            if (j < 0 || j >= cap_rank)
+                continue;
+            int64_t row = (int64_t)r * cap_rank + j;
+            rank_src_idx[row] = t;
+            if (!fp8) {
+                uint16_t* dst = (uint16_t*)recv_rank + row * H;
+                for (int h = 0; h < H; ++h)
+                    dst[h] = xr[h];
+                continue;
+            }
+            uint8_t* dst = (uint8_t*)recv_rank + row * H;
+            for (int g = 0; g < G; ++g) {
+                float amax = 0.0f;
+                for (int i = 0; i < 128; ++i) {
+                    float v = fabsf(oracle_bf16_to_f32(xr[128 * g + i]));
+                    if (v > amax)
+                        amax = v;
+                }
+                amax = fmaxf(amax, 1e-4f);
+                float scale = amax / 448.0f;
+                for (int i = 0; i < 128; ++i)
+                    dst[128 * g + i] = oracle_e4m3_encode(oracle_bf16_to_f32(xr[128 * g + i]) / scale);
+                scales_rank[row * G + g] = scale;
+            }
+        }
+    }
+}
+
+/*
+ * Rank combine: each rank returns one partial row per (token, rank) - the
+ * weighted sum over the token's experts on that rank, formed on the expert
+ * side - and
+ *   y[t][h] = bf16( sum over r = 0..R-1 ascending of float(rank_out[r][j][h]) )
+ * over the ranks with j = rank_slot[t][r] in [0, cap_rank), binary32
+ * accumulator from +0, one rounded add per rank.  A token in no rank gives +0.
+ */
+void oracle_rank_combine(const uint16_t* rank_out, int R, int cap_rank, int H,
+                         const int32_t* rank_slot, int T, uint16_t* y)
+{
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int r = 0; r < R; ++r) {
+                int j = rank_slot[(int64_t)t * R + r];
+                if (j < 0 || j >= cap_rank)
+                    continue;
+                acc = acc + oracle_bf16_to_f32(rank_out[((int64_t)r * cap_rank + j) * H + h]);
+            }
+            y[(int64_t)t * H + h] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
