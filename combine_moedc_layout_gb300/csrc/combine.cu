@@ -159,3 +159,128 @@ extern "C" int moedc_combine(const void* expert_out, int E, int cap, int H,
         static_cast<uint16_t*>(y), dev_status);
     return launch_status();
 }
+
+namespace moedc {
+
+constexpr int kCombine8Batch = 8;
+
+// Combine from e4m3 expert outputs: lane covers 16 consecutive channels
+// (one 16-byte load of codes per row, all in one 128-channel scale group).
+__global__ void __launch_bounds__(kCombineThreads, 2)
+combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restrict__ scales,
+                    bool scale_cols, int E, int cap, int H, const int32_t* __restrict__ topk_idx,
+                    const int32_t* __restrict__ slot, const float* __restrict__ topk_weights,
+                    int T, int K, uint16_t* __restrict__ y, int32_t* __restrict__ status)
+{
+    const int lane = threadIdx.x % kWarp;
+    const int G = H / 128;
+    const int nslice = (H + 511) / 512;
+    const int nwarps = gridDim.x * (blockDim.x / kWarp);
+    int gw = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
+    int t = gw / nslice, sl = gw - (gw / nslice) * nslice;
+    const int dt = nwarps / nslice, dsl = nwarps - dt * nslice;
+    bool bad = false;
+    for (; t < T;) {
+        int my_e = -1, my_s = -1;
+        float my_w = 0.0f;
+        if (lane < K) {
+            my_e = __ldg(topk_idx + (int64_t)t * K + lane);
+            my_s = __ldg(slot + (int64_t)t * K + lane);
+            my_w = __ldg(topk_weights + (int64_t)t * K + lane);
+            if (sl == 0 && (my_e < -1 || my_e >= E)) bad = true;
+        }
+        const int c0 = sl * 512 + lane * 16;
+        const bool act = c0 < H;
+        const int g = act ? c0 / 128 : 0;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int k0 = 0; k0 < K; k0 += kCombine8Batch) {
+            uint4 q[kCombine8Batch];
+            float sc[kCombine8Batch], wk[kCombine8Batch];
+            bool ok[kCombine8Batch];
+            // unconditional loads (skipped entries read row 0), all in flight together
+#pragma unroll
+            for (int j = 0; j < kCombine8Batch; ++j) {
+                const int k = k0 + j;
+                const int e = __shfl_sync(0xffffffffu, my_e, k & 31);
+                const int s = __shfl_sync(0xffffffffu, my_s, k & 31);
+                wk[j] = __shfl_sync(0xffffffffu, my_w, k & 31);
+                ok[j] = k < K && e >= 0 && e < E && s >= 0 && s < cap;
+                const int64_t row = ok[j] ? (int64_t)e * cap + s : 0;
+                const int64_t si = !ok[j] ? 0
+                                   : scale_cols ? ((int64_t)e * G + g) * cap + s
+                                                : row * G + g;
+                q[j] = ld_global_nc(reinterpret_cast<const uint4*>(expert_out + row * H +
+                                                                     (act ? c0 : 0)));
+                sc[j] = __ldg(scales + si);
+            }
+#pragma unroll
+            for (int j = 0; j < kCombine8Batch; ++j) {
+                if (!ok[j]) continue;
+                const uint32_t u[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a, b, c, d;
+                    e4m3x2_to_f32(u[i] & 0xffffu, a, b);
+                    e4m3x2_to_f32(u[i] >> 16, c, d);
+                    acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(wk[j], __fmul_rn(a, sc[j])));
+                    acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(wk[j], __fmul_rn(b, sc[j])));
+                    acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(wk[j], __fmul_rn(c, sc[j])));
+                    acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(wk[j], __fmul_rn(d, sc[j])));
+                }
+            }
+        }
+        if (act) {
+            uint16_t* dst = y + (int64_t)t * H + c0;
+            st_global_cs(reinterpret_cast<uint4*>(dst),
+                         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+            st_global_cs(reinterpret_cast<uint4*>(dst + 8),
+                         make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                    pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+        }
+        t += dt;
+        sl += dsl;
+        if (sl >= nslice) {
+            sl -= nslice;
+            t += 1;
+        }
+    }
+    if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+}
+
+}  // namespace moedc
+
+extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_scales,
+                                  int scale_layout, int E, int cap, int H,
+                                  const int32_t* topk_idx, const int32_t* slot,
+                                  const float* topk_weights, int T, int K, void* y,
+                                  int32_t* dev_status, cudaStream_t stream)
+{
+    using namespace moedc_host;
+    if (scale_layout != 0 && scale_layout != MOEDC_SCALES_COL_MAJOR) return MOEDC_ERR_ARG;
+    if (T < 0 || H < 128 || H % 128 != 0 || K < 1 || K > MOEDC_MAX_K || E < 1 ||
+        E > MOEDC_MAX_E || cap < 1)
+        return MOEDC_ERR_ARG;
+    if ((int64_t)E * cap * (H / 128) > INT32_MAX || (int64_t)T * (H / 512 + 1) > INT32_MAX / 2)
+        return MOEDC_ERR_ARG;
+    if (!expert_out || !expert_scales || !dev_status) return MOEDC_ERR_ARG;
+    if (T > 0 && (!topk_idx || !slot || !topk_weights || !y)) return MOEDC_ERR_ARG;
+    if (!aligned(expert_out, 16) || !aligned(y, 16) || !aligned(expert_scales, 4) ||
+        !aligned(topk_idx, 4) || !aligned(slot, 4) || !aligned(topk_weights, 4) ||
+        !aligned(dev_status, 4))
+        return MOEDC_ERR_ARG;
+    if (T == 0) return MOEDC_OK;
+    const int64_t items = (int64_t)T * ((H + 511) / 512);
+    int64_t blocks = (items + moedc::kCombineThreads / moedc::kWarp - 1) /
+                     (moedc::kCombineThreads / moedc::kWarp);
+    const int64_t resident =
+        resident_blocks((const void*)moedc::combine_e4m3_kernel, moedc::kCombineThreads, 0);
+    if (blocks > resident) blocks = resident;
+    clear_stale_error();
+    moedc::combine_e4m3_kernel<<<(int)blocks, moedc::kCombineThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(expert_out), expert_scales, scale_layout != 0, E, cap, H,
+        topk_idx, slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status);
+    return launch_status();
+}

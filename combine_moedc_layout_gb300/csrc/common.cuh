@@ -46,6 +46,16 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
     return r;
 }
 
+// Two e4m3 codes (low byte first) -> two binary32 values.  Exact: every e4m3
+// value is an f16 value, and f16 widens exactly.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two_codes, float& lo, float& hi)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((unsigned short)(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((unsigned short)(h2 >> 16)));
+}
+
 // Plain 16-byte global accesses.  Streaming stores: written rows are not
 // re-read by this kernel, so they should not displace reusable lines.
 __device__ __forceinline__ uint4 ld_global_nc(const uint4* p)
@@ -72,6 +82,11 @@ __device__ __forceinline__ void st_global_cs_f32(float* p, float v)
 // Host-side helpers shared by the entry points.
 namespace moedc_host {
 
+// out_dtype: MOEDC_BF16, MOEDC_FP8_E4M3, or MOEDC_FP8_E4M3 | MOEDC_SCALES_COL_MAJOR
+inline bool dtype_ok(int d)
+{
+    return d == MOEDC_BF16 || d == MOEDC_FP8_E4M3 || d == (MOEDC_FP8_E4M3 | MOEDC_SCALES_COL_MAJOR);
+}
 int sm_count();                 // multiprocessors of the current device
 // blocks of `kernel` resident on the whole current device at once
 int resident_blocks(const void* kernel, int threads, size_t smem);

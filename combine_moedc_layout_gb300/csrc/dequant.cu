@@ -12,22 +12,13 @@ namespace moedc {
 constexpr int kDequantThreads = 256;
 constexpr int kDequantSlice = 512;   // channels per warp item (16 per lane)
 
-// two e4m3 codes -> two binary32 values (exact: every e4m3 value is an f16 value)
-__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two_codes, float& lo, float& hi)
-{
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((unsigned short)(h2 & 0xffffu)));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((unsigned short)(h2 >> 16)));
-}
-
 // Work items are (filled row, 512-channel slice) pairs only: each block first
 // turns min(count[e], cap) into an exclusive prefix over experts in shared
 // memory, then a flat filled-row index f maps to its expert by binary search.
 __global__ void __launch_bounds__(kDequantThreads)
 dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ scales,
-                    const int32_t* __restrict__ num_tokens_per_expert, int E, int cap, int H,
-                    uint16_t* __restrict__ out)
+                    bool scale_cols, const int32_t* __restrict__ num_tokens_per_expert, int E,
+                    int cap, int H, uint16_t* __restrict__ out)
 {
     __shared__ int s_pref[MOEDC_MAX_E + 1];
     __shared__ int s_part[kDequantThreads / kWarp];
@@ -81,11 +72,14 @@ dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ 
             const int mid = (lo + hi + 1) >> 1;
             if (s_pref[mid] <= f) lo = mid; else hi = mid - 1;
         }
-        const int64_t row = (int64_t)lo * cap + (f - s_pref[lo]);
+        const int sidx = f - s_pref[lo];
+        const int64_t row = (int64_t)lo * cap + sidx;
         const int c0 = sl * kDequantSlice + lane * 16;
         if (c0 >= H) continue;
         const uint4 q = ld_global_nc(reinterpret_cast<const uint4*>(recv + row * H + c0));
-        const float sc = __ldg(scales + row * G + c0 / 128);
+        const int g = c0 / 128;
+        const float sc = __ldg(scales + (scale_cols ? ((int64_t)lo * G + g) * cap + sidx
+                                                    : row * G + g));
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
 #pragma unroll
@@ -104,11 +98,12 @@ dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ 
 
 }  // namespace moedc
 
-extern "C" int moedc_dequant_e4m3(const void* recv, const float* scales,
+extern "C" int moedc_dequant_e4m3(const void* recv, const float* scales, int scale_layout,
                                   const int32_t* num_tokens_per_expert, int E, int cap, int H,
                                   void* out_bf16, cudaStream_t stream)
 {
     using namespace moedc_host;
+    if (scale_layout != 0 && scale_layout != MOEDC_SCALES_COL_MAJOR) return MOEDC_ERR_ARG;
     if (E < 1 || E > MOEDC_MAX_E || cap < 1 || H < 128 || H % 128 != 0) return MOEDC_ERR_ARG;
     if ((int64_t)E * cap * ((H + 511) / 512) > INT32_MAX) return MOEDC_ERR_ARG;
     if (!recv || !scales || !num_tokens_per_expert || !out_bf16) return MOEDC_ERR_ARG;
@@ -124,7 +119,7 @@ extern "C" int moedc_dequant_e4m3(const void* recv, const float* scales,
     if (blocks > resident) blocks = resident;
     clear_stale_error();
     moedc::dequant_e4m3_kernel<<<(int)blocks, moedc::kDequantThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(recv), scales, num_tokens_per_expert, E, cap, H,
-        static_cast<uint16_t*>(out_bf16));
+        static_cast<const uint8_t*>(recv), scales, scale_layout != 0, num_tokens_per_expert, E,
+        cap, H, static_cast<uint16_t*>(out_bf16));
     return launch_status();
 }

@@ -19,7 +19,7 @@ namespace moedc {
 
 constexpr int kDispatchThreads = 256;
 
-template <bool kFp8>
+template <bool kFp8, bool kScaleCols>
 __global__ void __launch_bounds__(kDispatchThreads, MOEDC_DISPATCH_MINB)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
                 const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
@@ -60,7 +60,8 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
         SliceX nx_v;
         load_item(nxt, nx_row, nx_v);
         if (cur.sl == 0 && lane < K && my_row >= 0) src_idx[my_row] = cur.t;
-        store_slice<kFp8>(xv, H, cur.sl, lane, K, my_row, recv, scales);
+        const int64_t sbase = kScaleCols ? colmajor_scale_base(my_row, cap, H / 128) : 0;
+        store_slice<kFp8, kScaleCols>(xv, H, cur.sl, lane, K, my_row, recv, scales, sbase, cap);
         cur = nxt;
         my_row = nx_row;
         xv = nx_v;
@@ -88,13 +89,15 @@ static bool dispatch_args_ok(const void* x, int T, int H, const int32_t* topk_id
 {
     if (T < 0 || H < 8 || K < 1 || K > MOEDC_MAX_K || E < 1 || E > MOEDC_MAX_E || cap < 1)
         return false;
-    if (out_dtype != MOEDC_BF16 && out_dtype != MOEDC_FP8_E4M3) return false;
+    if (!dtype_ok(out_dtype)) return false;
+    out_dtype &= ~MOEDC_SCALES_COL_MAJOR;
     if (out_dtype == MOEDC_BF16 && H % 8 != 0) return false;
     if (out_dtype == MOEDC_FP8_E4M3 && H % 128 != 0) return false;
     if ((int64_t)E * cap > INT32_MAX) return false;
     if ((int64_t)T * ((H + 511) / 512) > INT32_MAX / 2) return false;
     if (!cnt || !recv || !src_idx || !dev_status) return false;
     if (out_dtype == MOEDC_FP8_E4M3 && !scales) return false;
+    if (out_dtype == MOEDC_FP8_E4M3 && (int64_t)E * cap * (H / 128) > INT32_MAX) return false;
     if (T > 0 && (!x || !topk_idx || !slot)) return false;
     if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(scales, 4) || !aligned(topk_idx, 4) ||
         !aligned(slot, 4) || !aligned(cnt, 4) || !aligned(src_idx, 4) || !aligned(dev_status, 4))
@@ -114,19 +117,26 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
     int64_t blocks = (items + warps_per_block - 1) / warps_per_block;
     const int64_t fill_blocks = (fill + moedc::kDispatchThreads - 1) / moedc::kDispatchThreads;
     if (blocks < fill_blocks) blocks = fill_blocks;
-    const void* fn = out_dtype == MOEDC_FP8_E4M3 ? (const void*)moedc::dispatch_kernel<true>
-                                                 : (const void*)moedc::dispatch_kernel<false>;
+    const bool cols = (out_dtype & MOEDC_SCALES_COL_MAJOR) != 0;
+    const int base = out_dtype & ~MOEDC_SCALES_COL_MAJOR;
+    const void* fn = base == MOEDC_BF16 ? (const void*)moedc::dispatch_kernel<false, false>
+                     : cols             ? (const void*)moedc::dispatch_kernel<true, true>
+                                        : (const void*)moedc::dispatch_kernel<true, false>;
     const int64_t resident = resident_blocks(fn, moedc::kDispatchThreads, 0);
     if (blocks > resident) blocks = resident;
     if (blocks < 1) blocks = 1;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
-    if (out_dtype == MOEDC_FP8_E4M3)
-        moedc::dispatch_kernel<true><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
+    if (base == MOEDC_BF16)
+        moedc::dispatch_kernel<false, false><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
+            xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
+            dev_status);
+    else if (cols)
+        moedc::dispatch_kernel<true, true><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
             xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
             dev_status);
     else
-        moedc::dispatch_kernel<false><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
+        moedc::dispatch_kernel<true, false><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
             xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
             dev_status);
     return launch_status();

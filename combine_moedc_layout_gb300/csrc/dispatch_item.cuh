@@ -78,8 +78,12 @@ __device__ __forceinline__ SliceX load_slice_fp8(const uint16_t* __restrict__ xr
     return v;
 }
 
+// kScaleCols: scales stored [E][G][cap] (group-major per expert) instead of
+// [E][cap][G]; lane k then also holds my_sbase = e * G * cap + s for entry k.
+template <bool kScaleCols>
 __device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slice, int lane,
-                                                int K, int my_row, uint8_t* __restrict__ recv,
+                                                int K, int my_row, int64_t my_sbase, int cap,
+                                                uint8_t* __restrict__ recv,
                                                 float* __restrict__ scales)
 {
     const int G = H / 128;
@@ -113,9 +117,14 @@ __device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slic
     const int g = c0 / 128;
     for (int k = 0; k < K; ++k) {
         const int row = __shfl_sync(0xffffffffu, my_row, k);
+        int64_t sbase = 0;
+        if (kScaleCols) sbase = __shfl_sync(0xffffffffu, my_sbase, k);
         if (row < 0 || !act) continue;
         st_global_cs(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), q);
-        if (leader) st_global_cs_f32(scales + (int64_t)row * G + g, sc);
+        if (leader) {
+            const int64_t si = kScaleCols ? sbase + (int64_t)g * cap : (int64_t)row * G + g;
+            st_global_cs_f32(scales + si, sc);
+        }
     }
 }
 
@@ -125,14 +134,25 @@ __device__ __forceinline__ SliceX load_slice(const uint16_t* xrow, int H, int sl
     return kFp8 ? load_slice_fp8(xrow, H, slice, lane) : load_slice_bf16(xrow, H, slice, lane);
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kScaleCols = false>
 __device__ __forceinline__ void store_slice(const SliceX& v, int H, int slice, int lane, int K,
-                                            int my_row, void* recv, float* scales)
+                                            int my_row, void* recv, float* scales,
+                                            int64_t my_sbase = 0, int cap = 0)
 {
     if (kFp8)
-        store_slice_fp8(v, H, slice, lane, K, my_row, static_cast<uint8_t*>(recv), scales);
+        store_slice_fp8<kScaleCols>(v, H, slice, lane, K, my_row, my_sbase, cap,
+                                    static_cast<uint8_t*>(recv), scales);
     else
         store_slice_bf16(v, H, slice, lane, K, my_row, static_cast<uint16_t*>(recv));
+}
+
+// e * G * cap + s: where entry (e, s)'s group-0 scale sits in [E][G][cap] scales
+__device__ __forceinline__ int64_t colmajor_scale_base(int row, int cap, int G)
+{
+    if (row < 0) return 0;
+    const int e = row / cap;
+    const int s = row - e * cap;
+    return (int64_t)e * G * cap + s;
 }
 
 // Destination row index e * cap + s of a routing entry, or -1 when the entry

@@ -17,7 +17,7 @@ namespace moedc {
 constexpr int kFusedThreads = 128;
 constexpr int kFusedWarps = kFusedThreads / kWarp;
 
-template <bool kFp8>
+template <bool kFp8, bool kScaleCols>
 __global__ void __launch_bounds__(kFusedThreads)
 fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              int T, int H, int K, int E, int R, int cap,
@@ -137,7 +137,8 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
             if (sl == 0 && my_row >= 0) src_idx[my_row] = t;
         }
         const SliceX v = load_slice<kFp8>(x + (int64_t)t * H, H, sl, lane);
-        store_slice<kFp8>(v, H, sl, lane, K, my_row, recv, scales);
+        const int64_t sbase = kScaleCols ? colmajor_scale_base(my_row, cap, H / 128) : 0;
+        store_slice<kFp8, kScaleCols>(v, H, sl, lane, K, my_row, recv, scales, sbase, cap);
     }
 }
 
@@ -153,15 +154,17 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
 {
     using namespace moedc_host;
     if (!layout_args_ok(T, K, E, R, cap)) return MOEDC_ERR_ARG;
-    if (H < 8 || (out_dtype == MOEDC_BF16 && H % 8 != 0) ||
-        (out_dtype == MOEDC_FP8_E4M3 && H % 128 != 0) ||
-        (out_dtype != MOEDC_BF16 && out_dtype != MOEDC_FP8_E4M3))
+    if (!dtype_ok(out_dtype)) return MOEDC_ERR_ARG;
+    const bool cols = (out_dtype & MOEDC_SCALES_COL_MAJOR) != 0;
+    const int base = out_dtype & ~MOEDC_SCALES_COL_MAJOR;
+    if (H < 8 || (base == MOEDC_BF16 && H % 8 != 0) || (base == MOEDC_FP8_E4M3 && H % 128 != 0))
         return MOEDC_ERR_ARG;
+    if (base == MOEDC_FP8_E4M3 && (int64_t)E * cap * (H / 128) > INT32_MAX) return MOEDC_ERR_ARG;
     if (!num_tokens_per_expert || !num_tokens_per_rank || !dev_status || !recv || !src_idx)
         return MOEDC_ERR_ARG;
     if ((int64_t)E * cap > INT32_MAX || (int64_t)T * ((H + 511) / 512) > INT32_MAX / 2)
         return MOEDC_ERR_ARG;
-    if (out_dtype == MOEDC_FP8_E4M3 && !scales) return MOEDC_ERR_ARG;
+    if (base == MOEDC_FP8_E4M3 && !scales) return MOEDC_ERR_ARG;
     if (T > 0 && (!x || !topk_idx || !is_token_in_rank || !slot)) return MOEDC_ERR_ARG;
     if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(scales, 4) || !aligned(topk_idx, 4) ||
         !aligned(slot, 4) || !aligned(num_tokens_per_expert, 4) ||
@@ -186,23 +189,25 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     int64_t blocks = (items + moedc::kFusedWarps - 1) / moedc::kFusedWarps;
     const int64_t fill_blocks = ((int64_t)E * cap + moedc::kFusedThreads - 1) / moedc::kFusedThreads;
     if (blocks < fill_blocks) blocks = fill_blocks;
-    const void* fn = out_dtype == MOEDC_FP8_E4M3
-                         ? (const void*)moedc::fused_layout_dispatch_kernel<true>
-                         : (const void*)moedc::fused_layout_dispatch_kernel<false>;
-    const int64_t resident = resident_blocks(
-        fn, moedc::kFusedThreads, (size_t)(2 * n + (moedc::kFusedWarps + 1) * E + R) * 4);
-    if (blocks > resident) blocks = resident;
-    if (blocks < 1) blocks = 1;
+    const void* fn = base == MOEDC_BF16
+                         ? (const void*)moedc::fused_layout_dispatch_kernel<false, false>
+                     : cols ? (const void*)moedc::fused_layout_dispatch_kernel<true, true>
+                            : (const void*)moedc::fused_layout_dispatch_kernel<true, false>;
     const size_t sm = (size_t)(2 * n + (moedc::kFusedWarps + 1) * E + R) * sizeof(int32_t);
+    const int64_t resident = resident_blocks(fn, moedc::kFusedThreads, sm);
+    if (blocks > resident) blocks = resident;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
-    if (out_dtype == MOEDC_FP8_E4M3)
-        moedc::fused_layout_dispatch_kernel<true><<<(int)blocks, moedc::kFusedThreads, sm, stream>>>(
-            xb, topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,
-            is_token_in_rank, slot, recv, scales, src_idx, dev_status);
+#define MOEDC_FUSED_LAUNCH(F, C)                                                                 \
+    moedc::fused_layout_dispatch_kernel<F, C><<<(int)blocks, moedc::kFusedThreads, sm, stream>>>( \
+        xb, topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,          \
+        is_token_in_rank, slot, recv, scales, src_idx, dev_status)
+    if (base == MOEDC_BF16)
+        MOEDC_FUSED_LAUNCH(false, false);
+    else if (cols)
+        MOEDC_FUSED_LAUNCH(true, true);
     else
-        moedc::fused_layout_dispatch_kernel<false><<<(int)blocks, moedc::kFusedThreads, sm, stream>>>(
-            xb, topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,
-            is_token_in_rank, slot, recv, scales, src_idx, dev_status);
+        MOEDC_FUSED_LAUNCH(true, false);
+#undef MOEDC_FUSED_LAUNCH
     return launch_status();
 }

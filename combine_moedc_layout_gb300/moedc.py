@@ -29,11 +29,12 @@ ERR_UNIMPLEMENTED = 6
 
 BF16 = 0
 FP8_E4M3 = 1
+SCALES_COL_MAJOR = 0x100    # OR into FP8_E4M3: scales stored [E, H/128, cap]
 
 EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes",
             "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
             "moedc_layout_static_scratch", "moedc_dequant_e4m3", "moedc_rank_layout",
-            "moedc_rank_dispatch", "moedc_rank_combine")
+            "moedc_rank_dispatch", "moedc_rank_combine", "moedc_combine_e4m3")
 
 STATIC_SCRATCH_BYTES = 1 << 20   # MOEDC_STATIC_SCRATCH_BYTES
 
@@ -78,7 +79,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_layout_dispatch.restype = I
     lib.moedc_layout_static_scratch.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P]
     lib.moedc_layout_static_scratch.restype = I
-    lib.moedc_dequant_e4m3.argtypes = [P, P, P, I, I, I, P, P]
+    lib.moedc_dequant_e4m3.argtypes = [P, P, I, P, I, I, I, P, P]
     lib.moedc_dequant_e4m3.restype = I
     lib.moedc_rank_layout.argtypes = [P, I, I, I, P, P, P]
     lib.moedc_rank_layout.restype = I
@@ -86,6 +87,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_rank_dispatch.restype = I
     lib.moedc_rank_combine.argtypes = [P, I, I, I, P, I, P, P]
     lib.moedc_rank_combine.restype = I
+    lib.moedc_combine_e4m3.argtypes = [P, P, I, I, I, I, P, P, P, I, I, P, P, P]
+    lib.moedc_combine_e4m3.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -160,9 +163,18 @@ def moedc_layout_dispatch(x, topk_idx, T, H, K, E, R, cap, out_dtype, num_tokens
         _p(src_idx), _p(workspace), workspace_bytes, _p(dev_status), _stream(stream))
 
 
-def moedc_dequant_e4m3(recv, scales, num_tokens_per_expert, E, cap, H, out, stream=None) -> int:
-    return load().moedc_dequant_e4m3(_p(recv), _p(scales), _p(num_tokens_per_expert), E, cap, H,
-                                     _p(out), _stream(stream))
+def moedc_dequant_e4m3(recv, scales, scale_layout, num_tokens_per_expert, E, cap, H, out,
+                       stream=None) -> int:
+    return load().moedc_dequant_e4m3(_p(recv), _p(scales), scale_layout,
+                                     _p(num_tokens_per_expert), E, cap, H, _p(out),
+                                     _stream(stream))
+
+
+def moedc_combine_e4m3(expert_out, expert_scales, scale_layout, E, cap, H, topk_idx, slot,
+                       topk_weights, T, K, y, dev_status, stream=None) -> int:
+    return load().moedc_combine_e4m3(_p(expert_out), _p(expert_scales), scale_layout, E, cap, H,
+                                     _p(topk_idx), _p(slot), _p(topk_weights), T, K, _p(y),
+                                     _p(dev_status), _stream(stream))
 
 
 def moedc_rank_layout(is_token_in_rank, T, R, cap_rank, rank_slot, dev_status, stream=None) -> int:
@@ -227,10 +239,11 @@ def layout(topk_idx: torch.Tensor, E: int, R: int, cap: int,
 
 def alloc_recv(E: int, cap: int, H: int, out_dtype: int, device):
     """recv [E,cap,H] (bf16, or e4m3 as torch.float8_e4m3fn), scales [E,cap,H/128]
-    (fp32, e4m3 only) and src_idx [E,cap]."""
-    if out_dtype == FP8_E4M3:
+    ([E,H/128,cap] with SCALES_COL_MAJOR; fp32, e4m3 only) and src_idx [E,cap]."""
+    if out_dtype & ~SCALES_COL_MAJOR == FP8_E4M3:
         recv = torch.empty((E, cap, H), dtype=torch.float8_e4m3fn, device=device)
-        scales = torch.empty((E, cap, H // 128), dtype=torch.float32, device=device)
+        shape = (E, H // 128, cap) if out_dtype & SCALES_COL_MAJOR else (E, cap, H // 128)
+        scales = torch.empty(shape, dtype=torch.float32, device=device)
     else:
         recv = torch.empty((E, cap, H), dtype=torch.bfloat16, device=device)
         scales = None
@@ -289,14 +302,29 @@ def layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int, cap
 
 
 def dequant_e4m3(recv: torch.Tensor, scales: torch.Tensor, num_tokens_per_expert: torch.Tensor,
-                 out: torch.Tensor | None = None) -> torch.Tensor:
+                 out: torch.Tensor | None = None, scale_layout: int = 0) -> torch.Tensor:
     """bf16 [E, cap, H] view of an e4m3 receive buffer (filled rows only)."""
     E, cap, H = recv.shape
     if out is None:
         out = torch.zeros((E, cap, H), dtype=torch.bfloat16, device=recv.device)
-    _check(moedc_dequant_e4m3(recv, scales, num_tokens_per_expert, E, cap, H, out),
+    _check(moedc_dequant_e4m3(recv, scales, scale_layout, num_tokens_per_expert, E, cap, H, out),
            "moedc_dequant_e4m3")
     return out
+
+
+def combine_e4m3(expert_out: torch.Tensor, expert_scales: torch.Tensor, topk_idx: torch.Tensor,
+                 slot: torch.Tensor, topk_weights: torch.Tensor, scale_layout: int = 0,
+                 status: torch.Tensor | None = None) -> torch.Tensor:
+    """Combine from e4m3 expert outputs [E, cap, H] with per-128 fp32 scales."""
+    _need(topk_weights, torch.float32, "topk_weights")
+    E, cap, H = expert_out.shape
+    T, K = topk_idx.shape
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=expert_out.device)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=expert_out.device)
+    _check(moedc_combine_e4m3(expert_out, expert_scales, scale_layout, E, cap, H, topk_idx, slot,
+                              topk_weights, T, K, y, status), "moedc_combine_e4m3")
+    return y
 
 
 def rank_layout(lay: Layout, cap_rank: int) -> torch.Tensor:

@@ -89,6 +89,12 @@ typedef enum {
 
 typedef enum { MOEDC_BF16 = 0, MOEDC_FP8_E4M3 = 1 } moedc_dtype;
 
+/* OR-ed into the out_dtype of moedc_dispatch / moedc_layout_dispatch with
+ * MOEDC_FP8_E4M3: the fp32 scales are stored [E][G][cap] (per expert, one
+ * contiguous run of cap scales per 128-channel group, the order a grouped FP8
+ * GEMM reads per K-block) instead of [E][cap][G].  Codes are unchanged. */
+#define MOEDC_SCALES_COL_MAJOR 0x100
+
 /* Limits checked on the host (MOEDC_ERR_ARG beyond them). */
 #define MOEDC_MAX_K 32
 #define MOEDC_MAX_E 1024
@@ -157,7 +163,8 @@ MOEDC_EXPORT int moedc_layout_static_scratch(const int32_t* topk_idx, int T, int
  * For every entry (t, k) with expert e in [0, E) and slot s in [0, cap):
  *   src_idx[e][s] = t
  *   MOEDC_BF16:     recv[e][s][:] = x[t][:]  (bit copy; recv is bf16)
- *   MOEDC_FP8_E4M3: per group g of 128 channels, a = max |x[t][128g+i]|,
+ *   MOEDC_FP8_E4M3 (optionally | MOEDC_SCALES_COL_MAJOR, see above):
+ *                   per group g of 128 channels, a = max |x[t][128g+i]|,
  *                   a = max(a, 1e-4f), sc = a / 448 (IEEE binary32 division),
  *                   recv[e][s][128g+i] = e4m3fn(x / sc) with one binary32
  *                   division and round-to-nearest-even, saturating to +-448;
@@ -199,11 +206,27 @@ MOEDC_EXPORT int moedc_combine(const void* expert_out, int E, int cap, int H,
  * and channel h of group g = h / 128:
  *   out[e][s][h] = bf16_rne( float(recv[e][s][h]) * scales[e][s][g] )
  * with one binary32 multiply.  Rows past an expert's count are not written.
+ * scale_layout: 0 for scales [E][cap][G], MOEDC_SCALES_COL_MAJOR for [E][G][cap].
  * recv and out must be 16-byte aligned; H % 128 == 0.  No data errors.
  */
-MOEDC_EXPORT int moedc_dequant_e4m3(const void* recv, const float* scales,
+MOEDC_EXPORT int moedc_dequant_e4m3(const void* recv, const float* scales, int scale_layout,
                  const int32_t* num_tokens_per_expert, int E, int cap, int H,
                  void* out_bf16, cudaStream_t stream);
+
+/*
+ * Combine from e4m3 expert outputs with per-128-channel fp32 scales (the
+ * same format dispatch produces; scale_layout as for moedc_dequant_e4m3):
+ *   y[t][h] = bf16_rne( sum over k ascending of
+ *                       w[t][k] * (float(expert_out[e][s][h]) * scale(e, s, h/128)) )
+ * binary32 accumulator from +0, each product rounded, never fused; masked,
+ * out-of-range and dropped entries skipped.  Reads 1 byte per element
+ * instead of 2.  expert_out and y 16-byte aligned, H % 128 == 0.
+ * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE.
+ */
+MOEDC_EXPORT int moedc_combine_e4m3(const void* expert_out, const float* expert_scales,
+                 int scale_layout, int E, int cap, int H, const int32_t* topk_idx,
+                 const int32_t* slot, const float* topk_weights, int T, int K, void* y,
+                 int32_t* dev_status, cudaStream_t stream);
 
 /*
  * Rank-major packed receive [UCCL749 title: tokens batched per destination].

@@ -67,6 +67,8 @@ def _load():
     lib.oracle_rank_layout.restype = I
     lib.oracle_rank_dispatch.argtypes = [P, I, I, P, I, I, I, P, P, P]
     lib.oracle_rank_combine.argtypes = [P, I, I, I, P, I, P]
+    lib.oracle_combine_e4m3.argtypes = [P, P, I, I, I, I, P, P, P, I, I, P]
+    lib.oracle_combine_e4m3.restype = I
     _lib = lib
     return lib
 
@@ -200,3 +202,21 @@ def rank_combine(rank_out: np.ndarray, rank_slot: np.ndarray) -> np.ndarray:
     y = np.empty((T, H), np.uint16)
     _load().oracle_rank_combine(_ptr(rank_out), R, cap_rank, H, _ptr(rank_slot), T, _ptr(y))
     return y
+
+
+def combine_e4m3(expert_out: np.ndarray, expert_scales: np.ndarray, topk_idx: np.ndarray,
+                 slot: np.ndarray, topk_weights: np.ndarray, scale_cols: bool = False) -> dict:
+    """expert_out: e4m3 codes uint8 [E, cap, H]; expert_scales float32 [E, cap, H/128]
+    (or [E, H/128, cap] with scale_cols).  Returns y (bf16 bits [T, H]) and status."""
+    expert_out = np.ascontiguousarray(expert_out, dtype=np.uint8)
+    expert_scales = np.ascontiguousarray(expert_scales, dtype=np.float32)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    E, cap, H = expert_out.shape
+    T, K = topk_idx.shape
+    y = np.empty((T, H), np.uint16)
+    status = _load().oracle_combine_e4m3(_ptr(expert_out), _ptr(expert_scales),
+                                         1 if scale_cols else 0, E, cap, H, _ptr(topk_idx),
+                                         _ptr(slot), _ptr(topk_weights), T, K, _ptr(y))
+    return dict(y=y, status=status)

@@ -436,3 +436,48 @@ void oracle_rank_combine(const uint16_t* rank_out, int R, int cap_rank, int H,
         }
     }
 }
+
+/* -------------------------------------------------------- e4m3 combine */
+/*
+ * Combine from e4m3 expert outputs with per-128-channel fp32 scales
+ * (expert_scales row-major [E][cap][G], or [E][G][cap] when scale_cols != 0).
+ * For every token t and channel h, group g = h / 128:
+ *   acc = 0.0f
+ *   for k = 0 .. K-1 ascending, skipping masked / out-of-range / dropped entries:
+ *       v   = decode(q[e][s][h]) * scale(e, s, g)    (binary32 multiply)
+ *       p   = w[t][k] * v                            (binary32 multiply)
+ *       acc = acc + p                                (binary32 add)
+ *   y[t][h] = bf16(acc), nearest even.
+ */
+int oracle_combine_e4m3(const uint8_t* expert_out, const float* expert_scales, int scale_cols,
+                        int E, int cap, int H, const int32_t* topk_idx, const int32_t* slot,
+                        const float* topk_weights, int T, int K, uint16_t* y)
+{
+    int status = ORACLE_OK;
+    int G = H / 128;
+    for (int t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int e = topk_idx[(int64_t)t * K + k];
+            if (e < -1 || e >= E)
+                status = raise_status(status, ORACLE_ERR_EXPERT_RANGE);
+        }
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            int g = h / 128;
+            for (int k = 0; k < K; ++k) {
+                int e = topk_idx[(int64_t)t * K + k];
+                int s = slot[(int64_t)t * K + k];
+                if (!entry_valid(e, s, E, cap))
+                    continue;
+                int64_t row = (int64_t)e * cap + s;
+                float sc = scale_cols ? expert_scales[((int64_t)e * G + g) * cap + s]
+                                      : expert_scales[row * G + g];
+                float v = oracle_e4m3_decode(expert_out[row * H + h]) * sc;
+                float p = topk_weights[(int64_t)t * K + k] * v;
+                acc = acc + p;
+            }
+            y[(int64_t)t * H + h] = oracle_f32_to_bf16(acc);
+        }
+    }
+    return status;
+}

@@ -92,6 +92,15 @@ def test_argument_errors_return_before_cuda(lib):
         moedc.ERR_ARG
     assert lib.moedc_combine(fake, 8, 4, 128, fake, fake, fake, 4, 2, None, fake, None) == \
         moedc.ERR_ARG
+    # e4m3 combine / dequant: unknown scale layout, H % 128 != 0; dispatch: unknown dtype bits
+    assert lib.moedc_combine_e4m3(fake, fake, 7, 8, 4, 256, fake, fake, fake, 4, 2, fake, fake,
+                                  None) == moedc.ERR_ARG
+    assert lib.moedc_combine_e4m3(fake, fake, 0, 8, 4, 200, fake, fake, fake, 4, 2, fake, fake,
+                                  None) == moedc.ERR_ARG
+    assert lib.moedc_dequant_e4m3(fake, fake, 3, fake, 8, 4, 256, fake, None) == moedc.ERR_ARG
+    assert lib.moedc_dispatch(fake, 4, 256, fake, fake, fake, 2, 8, 4,
+                              moedc.BF16 | moedc.SCALES_COL_MAJOR, fake, fake, fake, fake,
+                              None) == moedc.ERR_ARG
     # fused: a shape past the single-launch layout (> 65536 entries) without workspace
     assert lib.moedc_layout_dispatch(fake, fake, 9000, 256, 8, 64, 8, 1200, moedc.BF16, fake,
                                      fake, fake, fake, fake, None, fake, None, 0, fake,

@@ -295,3 +295,55 @@ def test_dispatch_then_dequant_error_bound():
             # e4m3 half-ulp of x/s times s, plus the bf16 rounding of the product
             bound = 0.5 * _e4m3_ulp(x[t] / sc) * sc * (1 + 2.0**-20) + np.abs(y) * 2.0**-8
             assert (np.abs(y - x[t]) <= bound).all()
+
+
+# ------------------------------------------------------------ e4m3 combine
+
+def test_combine_e4m3_k1_unit_weight_equals_dequant():
+    """One entry with weight 1: the sum is the dequantised value itself."""
+    c = synth.make_random_case(71, T=60, H=256, K=1, E=6, R=3, cap=None, dtype=synth.FP8_E4M3)
+    lay = _run_layout(c)
+    d = oracle.dispatch(c.x, c.topk_idx, lay["slot"], c.E, c.cap, fp8=True)
+    w = np.ones((c.T, 1), np.float32)
+    y = oracle.combine_e4m3(d["recv"], d["scales"], c.topk_idx, lay["slot"], w)["y"]
+    deq = oracle.dequant_e4m3(d["recv"], d["scales"], lay["num_tokens_per_expert"])
+    for t in range(c.T):
+        np.testing.assert_array_equal(y[t], deq[c.topk_idx[t, 0], lay["slot"][t, 0]])
+
+
+def test_combine_e4m3_column_major_scales_same_result():
+    c = synth.make_case("low8")
+    lay = _run_layout(c)
+    d = oracle.dispatch(c.x, c.topk_idx, lay["slot"], c.E, c.cap, fp8=True)
+    a = oracle.combine_e4m3(d["recv"], d["scales"], c.topk_idx, lay["slot"], c.topk_weights)
+    cm = np.ascontiguousarray(d["scales"].transpose(0, 2, 1))           # [E, G, cap]
+    b = oracle.combine_e4m3(d["recv"], cm, c.topk_idx, lay["slot"], c.topk_weights,
+                            scale_cols=True)
+    np.testing.assert_array_equal(a["y"], b["y"])
+
+
+def test_combine_e4m3_identity_round_trip_near_x():
+    """Identity experts (expert output = the dispatched e4m3 rows) and weights
+    renormalised to sum 1 return x within the e4m3 error of each group."""
+    c = synth.make_case("low16")
+    w = c.topk_weights / c.topk_weights.sum(axis=1, keepdims=True, dtype=np.float32)
+    lay = _run_layout(c)
+    d = oracle.dispatch(c.x, c.topk_idx, lay["slot"], c.E, c.cap, fp8=True)
+    y = oracle.combine_e4m3(d["recv"], d["scales"], c.topk_idx, lay["slot"],
+                            w.astype(np.float32))["y"]
+    x = _bf16(c.x).astype(np.float64)
+    yy = _bf16(y).astype(np.float64)
+    amax = np.abs(x).reshape(c.T, -1, 128).max(axis=2).repeat(128, axis=1)
+    assert (np.abs(yy - x) <= amax * 2.0**-4 + np.abs(x) * 2.0**-7).all()
+
+
+def test_combine_e4m3_closed_form():
+    # codes 0x7E (448) and 0x38 (1.0) with scales 0.5 and 4; weights 0.25, 0.5
+    q = np.array([[[0x7E] * 128], [[0x38] * 128]], np.uint8)                # [E=2, cap=1, H=128]
+    s = np.array([[[0.5]], [[4.0]]], np.float32)
+    idx = np.array([[0, 1]], np.int32)
+    slot = np.array([[0, 0]], np.int32)
+    w = np.array([[0.25, 0.5]], np.float32)
+    y = oracle.combine_e4m3(q, s, idx, slot, w)["y"]
+    # 0.25 * 224 + 0.5 * 4 = 58 exactly
+    assert (_bf16(y) == np.float32(58.0)).all()
