@@ -58,23 +58,31 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t two_codes, float& lo, flo
 
 // Plain 16-byte global accesses.  Streaming stores: written rows are not
 // re-read by this kernel, so they should not displace reusable lines.
+#ifndef MOEDC_LD_POLICY
+#define MOEDC_LD_POLICY ".L1::no_allocate"
+#endif
+
 __device__ __forceinline__ uint4 ld_global_nc(const uint4* p)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc" MOEDC_LD_POLICY ".v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
+#ifndef MOEDC_ST_POLICY
+#define MOEDC_ST_POLICY ".cs"
+#endif
+
 __device__ __forceinline__ void st_global_cs(uint4* p, uint4 v)
 {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+    asm volatile("st.global" MOEDC_ST_POLICY ".v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
 __device__ __forceinline__ void st_global_cs_f32(float* p, float v)
 {
-    asm volatile("st.global.cs.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+    asm volatile("st.global" MOEDC_ST_POLICY ".f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
 }
 
 }  // namespace moedc
