@@ -36,6 +36,7 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
                const float* __restrict__ topk_weights, int T, int K,
                uint16_t* __restrict__ y, int32_t* __restrict__ status)
 {
+    pdl_enter();
     const int lane = threadIdx.x % kWarp;
     const int nslice = (H + kCombineSlice - 1) / kCombineSlice;
     const int64_t items = (int64_t)T * nslice;
@@ -154,8 +155,7 @@ extern "C" int moedc_combine(const void* expert_out, int E, int cap, int H,
         resident_blocks((const void*)moedc::combine_kernel, moedc::kCombineThreads, 0);
     if (blocks > resident) blocks = resident;
     clear_stale_error();
-    moedc::combine_kernel<<<(int)blocks, moedc::kCombineThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(expert_out), E, cap, H, topk_idx, slot, topk_weights, T, K,
+    launch(moedc::combine_kernel, (int)blocks, moedc::kCombineThreads, 0, stream, static_cast<const uint16_t*>(expert_out), E, cap, H, topk_idx, slot, topk_weights, T, K,
         static_cast<uint16_t*>(y), dev_status);
     return launch_status();
 }
@@ -172,6 +172,7 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
                     const int32_t* __restrict__ slot, const float* __restrict__ topk_weights,
                     int T, int K, uint16_t* __restrict__ y, int32_t* __restrict__ status)
 {
+    pdl_enter();
     const int lane = threadIdx.x % kWarp;
     const int G = H / 128;
     const int nslice = (H + 511) / 512;
@@ -279,8 +280,7 @@ extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_sc
         resident_blocks((const void*)moedc::combine_e4m3_kernel, moedc::kCombineThreads, 0);
     if (blocks > resident) blocks = resident;
     clear_stale_error();
-    moedc::combine_e4m3_kernel<<<(int)blocks, moedc::kCombineThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(expert_out), expert_scales, scale_layout != 0, E, cap, H,
+    launch(moedc::combine_e4m3_kernel, (int)blocks, moedc::kCombineThreads, 0, stream, static_cast<const uint8_t*>(expert_out), expert_scales, scale_layout != 0, E, cap, H,
         topk_idx, slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status);
     return launch_status();
 }

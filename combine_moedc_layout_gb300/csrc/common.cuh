@@ -85,6 +85,25 @@ __device__ __forceinline__ void st_global_cs_f32(float* p, float v)
     asm volatile("st.global" MOEDC_ST_POLICY ".f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
 }
 
+#ifndef MOEDC_PDL
+#define MOEDC_PDL 1
+#endif
+
+// Programmatic dependent launch.  Every kernel of the library starts here: it
+// waits (in hardware) until the previous kernel in the stream has completed
+// and its memory is visible - a no-op when that launch carried no
+// programmatic dependency - and then lets the next kernel in the stream start
+// launching, so its blocks are scheduled while this one drains.  The next
+// kernel can only launch once every block of this one has passed this point,
+// so its waiting blocks never keep a block of this grid from being scheduled.
+__device__ __forceinline__ void pdl_enter()
+{
+#if MOEDC_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
 }  // namespace moedc
 
 // Host-side helpers shared by the entry points.
@@ -105,6 +124,26 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 // that launch_status() reports only the launch that follows it.
 inline void clear_stale_error() { (void)cudaGetLastError(); }
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? MOEDC_OK : MOEDC_ERR_CUDA; }
+
+// Launch with the programmatic-stream-serialisation attribute (see
+// pdl_enter); a failed launch is left in the runtime's last-error state for
+// launch_status() to report.
+template <typename... KArgs, typename... Args>
+inline void launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = MOEDC_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Layout geometry: tokens per thread block of the layout kernels.
 struct LayoutGeom {

@@ -20,6 +20,7 @@ dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ 
                     bool scale_cols, const int32_t* __restrict__ num_tokens_per_expert, int E,
                     int cap, int H, uint16_t* __restrict__ out)
 {
+    pdl_enter();
     __shared__ int s_pref[MOEDC_MAX_E + 1];
     __shared__ int s_part[kDequantThreads / kWarp];
     const int lane = threadIdx.x % kWarp;
@@ -118,8 +119,7 @@ extern "C" int moedc_dequant_e4m3(const void* recv, const float* scales, int sca
         resident_blocks((const void*)moedc::dequant_e4m3_kernel, moedc::kDequantThreads, 0);
     if (blocks > resident) blocks = resident;
     clear_stale_error();
-    moedc::dequant_e4m3_kernel<<<(int)blocks, moedc::kDequantThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(recv), scales, scale_layout != 0, num_tokens_per_expert, E,
+    launch(moedc::dequant_e4m3_kernel, (int)blocks, moedc::kDequantThreads, 0, stream, static_cast<const uint8_t*>(recv), scales, scale_layout != 0, num_tokens_per_expert, E,
         cap, H, static_cast<uint16_t*>(out_bf16));
     return launch_status();
 }

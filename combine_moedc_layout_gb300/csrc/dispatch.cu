@@ -27,6 +27,7 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
                 void* __restrict__ recv, float* __restrict__ scales,
                 int32_t* __restrict__ src_idx, int32_t* __restrict__ status)
 {
+    pdl_enter();
     const int lane = threadIdx.x % kWarp;
     const int nslice = (H + kSlice - 1) / kSlice;
     const int nwarps = gridDim.x * (blockDim.x / kWarp);
@@ -128,16 +129,13 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
     if (base == MOEDC_BF16)
-        moedc::dispatch_kernel<false, false><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
-            xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
+        launch(moedc::dispatch_kernel<false, false>, (int)blocks, moedc::kDispatchThreads, 0, stream, xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
             dev_status);
     else if (cols)
-        moedc::dispatch_kernel<true, true><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
-            xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
+        launch(moedc::dispatch_kernel<true, true>, (int)blocks, moedc::kDispatchThreads, 0, stream, xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
             dev_status);
     else
-        moedc::dispatch_kernel<true, false><<<(int)blocks, moedc::kDispatchThreads, 0, stream>>>(
-            xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
+        launch(moedc::dispatch_kernel<true, false>, (int)blocks, moedc::kDispatchThreads, 0, stream, xb, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap, recv, scales, src_idx,
             dev_status);
     return launch_status();
 }

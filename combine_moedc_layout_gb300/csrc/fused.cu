@@ -27,6 +27,7 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
                              void* __restrict__ recv, float* __restrict__ scales,
                              int32_t* __restrict__ src_idx, int32_t* __restrict__ status)
 {
+    pdl_enter();
     extern __shared__ int32_t smem[];
     const int n = T * K;
     int32_t* s_idx = smem;                      // [n]
@@ -199,7 +200,7 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
 #define MOEDC_FUSED_LAUNCH(F, C)                                                                 \
-    moedc::fused_layout_dispatch_kernel<F, C><<<(int)blocks, moedc::kFusedThreads, sm, stream>>>( \
+    launch(moedc::fused_layout_dispatch_kernel<F, C>, (int)blocks, moedc::kFusedThreads, sm, stream, \
         xb, topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,          \
         is_token_in_rank, slot, recv, scales, src_idx, dev_status)
     if (base == MOEDC_BF16)

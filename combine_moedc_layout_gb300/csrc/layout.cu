@@ -71,6 +71,7 @@ layout_sweep_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, i
                     uint8_t* __restrict__ is_token_in_rank, int32_t* __restrict__ slot,
                     int32_t* __restrict__ status)
 {
+    pdl_enter();
     __shared__ int32_t s_warp[kSweepWarps];
     __shared__ int32_t s_total;
     const int tid = threadIdx.x;
@@ -176,6 +177,7 @@ layout_count_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, i
                     int32_t* __restrict__ ws_hist, int32_t* __restrict__ ws_rank,
                     int32_t* __restrict__ status)
 {
+    pdl_enter();
     extern __shared__ int32_t smem[];
     int32_t* s_idx = smem;                // [tpc * K]
     int32_t* s_hist = s_idx + tpc * K;    // [E]
@@ -219,6 +221,7 @@ layout_assign_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, 
                      uint8_t* __restrict__ is_token_in_rank, int32_t* __restrict__ slot,
                      int32_t* __restrict__ status)
 {
+    pdl_enter();
     extern __shared__ int32_t smem[];
     int32_t* s_idx = smem;                          // [tpc * K]
     int32_t* s_whist = s_idx + tpc * K;             // [kLayoutWarps][E]
@@ -378,8 +381,7 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
     if (g.sweep) {
         const bool vec_ok = aligned(topk_idx, 16);
         clear_stale_error();
-        moedc::layout_sweep_kernel<<<g.blocks, moedc::kSweepThreads, 0, stream>>>(
-            topk_idx, T, K, E, R, cap, vec_ok, num_tokens_per_expert, num_tokens_per_rank,
+        launch(moedc::layout_sweep_kernel, g.blocks, moedc::kSweepThreads, 0, stream, topk_idx, T, K, E, R, cap, vec_ok, num_tokens_per_expert, num_tokens_per_rank,
             is_token_in_rank, slot, dev_status);
         return launch_status();
     }
@@ -390,16 +392,14 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
         if (ensure_smem_attr((const void*)moedc::layout_count_kernel, sm) != MOEDC_OK)
             return MOEDC_ERR_CUDA;
         clear_stale_error();
-        moedc::layout_count_kernel<<<g.blocks, moedc::kLayoutThreads, sm, stream>>>(
-            topk_idx, T, K, E, R, g.tpc, ws_hist, ws_rank, dev_status);
+        launch(moedc::layout_count_kernel, g.blocks, moedc::kLayoutThreads, sm, stream, topk_idx, T, K, E, R, g.tpc, ws_hist, ws_rank, dev_status);
         if (launch_status() != MOEDC_OK) return MOEDC_ERR_CUDA;
     }
     const size_t sm = moedc::assign_smem(g.tpc, K, E, R);
     if (ensure_smem_attr((const void*)moedc::layout_assign_kernel, sm) != MOEDC_OK)
         return MOEDC_ERR_CUDA;
     clear_stale_error();
-    moedc::layout_assign_kernel<<<g.blocks, moedc::kLayoutThreads, sm, stream>>>(
-        topk_idx, T, K, E, R, cap, g.tpc, ws_hist, ws_rank, num_tokens_per_expert,
+    launch(moedc::layout_assign_kernel, g.blocks, moedc::kLayoutThreads, sm, stream, topk_idx, T, K, E, R, cap, g.tpc, ws_hist, ws_rank, num_tokens_per_expert,
         num_tokens_per_rank, is_token_in_rank, slot, dev_status);
     return launch_status();
 }

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kRankLayoutThreads)
 rank_layout_kernel(const uint8_t* __restrict__ is_token_in_rank, int T, int R, int cap_rank,
                    int32_t* __restrict__ rank_slot, int32_t* __restrict__ status)
 {
+    pdl_enter();
     __shared__ int s_warp[kRankLayoutWarps];
     __shared__ int s_total;
     const int r = blockIdx.x;
@@ -84,6 +85,7 @@ rank_dispatch_kernel(const uint16_t* __restrict__ x, int T, int H,
                      void* __restrict__ recv_rank, float* __restrict__ scales_rank,
                      int32_t* __restrict__ rank_src_idx)
 {
+    pdl_enter();
     const int lane = threadIdx.x % kWarp;
     const int nslice = (H + kSlice - 1) / kSlice;
     const int nwarps = gridDim.x * (blockDim.x / kWarp);
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(kRankThreads, 2)
 rank_combine_kernel(const uint16_t* __restrict__ rank_out, int R, int cap_rank, int H,
                     const int32_t* __restrict__ rank_slot, int T, uint16_t* __restrict__ y)
 {
+    pdl_enter();
     const int lane = threadIdx.x % kWarp;
     const int nslice = (H + 511) / 512;
     const int nwarps = gridDim.x * (blockDim.x / kWarp);
@@ -195,8 +198,7 @@ extern "C" int moedc_rank_layout(const uint8_t* is_token_in_rank, int T, int R, 
     if (!aligned(rank_slot, 4) || !aligned(dev_status, 4)) return MOEDC_ERR_ARG;
     if (T == 0) return MOEDC_OK;
     clear_stale_error();
-    moedc::rank_layout_kernel<<<R, moedc::kRankLayoutThreads, 0, stream>>>(
-        is_token_in_rank, T, R, cap_rank, rank_slot, dev_status);
+    launch(moedc::rank_layout_kernel, R, moedc::kRankLayoutThreads, 0, stream, is_token_in_rank, T, R, cap_rank, rank_slot, dev_status);
     return launch_status();
 }
 
@@ -232,12 +234,10 @@ extern "C" int moedc_rank_dispatch(const void* x, int T, int H, const int32_t* r
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
     if (out_dtype == MOEDC_FP8_E4M3)
-        moedc::rank_dispatch_kernel<true><<<(int)blocks, moedc::kRankThreads, 0, stream>>>(
-            xb, T, H, rank_slot, num_tokens_per_rank, R, cap_rank, recv_rank, scales_rank,
+        launch(moedc::rank_dispatch_kernel<true>, (int)blocks, moedc::kRankThreads, 0, stream, xb, T, H, rank_slot, num_tokens_per_rank, R, cap_rank, recv_rank, scales_rank,
             rank_src_idx);
     else
-        moedc::rank_dispatch_kernel<false><<<(int)blocks, moedc::kRankThreads, 0, stream>>>(
-            xb, T, H, rank_slot, num_tokens_per_rank, R, cap_rank, recv_rank, scales_rank,
+        launch(moedc::rank_dispatch_kernel<false>, (int)blocks, moedc::kRankThreads, 0, stream, xb, T, H, rank_slot, num_tokens_per_rank, R, cap_rank, recv_rank, scales_rank,
             rank_src_idx);
     return launch_status();
 }
@@ -260,8 +260,7 @@ extern "C" int moedc_rank_combine(const void* rank_out, int R, int cap_rank, int
         resident_blocks((const void*)moedc::rank_combine_kernel, moedc::kRankThreads, 0);
     if (blocks > resident) blocks = resident;
     clear_stale_error();
-    moedc::rank_combine_kernel<<<(int)blocks, moedc::kRankThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(rank_out), R, cap_rank, H, rank_slot, T,
+    launch(moedc::rank_combine_kernel, (int)blocks, moedc::kRankThreads, 0, stream, static_cast<const uint16_t*>(rank_out), R, cap_rank, H, rank_slot, T,
         static_cast<uint16_t*>(y));
     return launch_status();
 }
