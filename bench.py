@@ -606,40 +606,93 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                 peak_src else peak_src, "traffic": ncu_traffic(kname),
                 "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
 
-    # ---- end to end through the public API with host buffers
-    e2e_steps = max(3, min(20, K_steps))
+    # ---- end to end through the public API with host buffers.  A caller that
+    # streams batches overlaps the next batch's host->device copies with this
+    # batch's kernels: two device input sets, the copies split over several
+    # copy streams, y and the counts copied back on their own stream.  Every
+    # step still copies all of its inputs in and its result out.
+    e2e_steps = max(4, min(20, K_steps))
+    n_copy = 4
     h_x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
     h_idx = torch.from_numpy(c.topk_idx).pin_memory()
     h_w = torch.from_numpy(c.topk_weights).pin_memory()
     h_eo = torch.from_numpy(eo_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_y = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_cnt = torch.empty(E, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_idx, h_w, h_eo))
-    d2h = h_y.numel() * 2 + h_cnt.numel() * 4
+    h_ins = (h_x, h_idx, h_w, h_eo)
+    h_outs = [(torch.empty((T, H), dtype=torch.bfloat16).pin_memory(),
+               torch.empty(E, dtype=torch.int32).pin_memory()) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_ins)
+    d2h = h_outs[0][0].numel() * 2 + h_outs[0][1].numel() * 4
+    d_ins = [(x, idx, w, eo), tuple(torch.empty_like(t) for t in (x, idx, w, eo))]
+    d_outs = [(y, cnt), (torch.empty_like(y), torch.empty_like(cnt))]
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(n_copy)]
+    back_stream = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [[ev() for _ in range(n_copy)] for _ in range(2)]
+    comp_done = [ev() for _ in range(2)]
+    out_done = [ev() for _ in range(2)]
+    for e_ in comp_done + out_done:
+        e_.record(stream)
 
-    def e2e_step():
-        x.copy_(h_x, non_blocking=True)
-        idx.copy_(h_idx, non_blocking=True)
-        w.copy_(h_w, non_blocking=True)
-        eo.copy_(h_eo, non_blocking=True)
-        step()
-        h_y.copy_(y, non_blocking=True)
-        h_cnt.copy_(cnt, non_blocking=True)
+    def issue_h2d(b):
+        for j, cs in enumerate(copy_streams):
+            cs.wait_event(comp_done[b])           # the kernels two steps back are done with set b
+            with torch.cuda.stream(cs):
+                for src, dst in zip(h_ins, d_ins[b]):
+                    fs, fd = src.view(-1), dst.view(-1)
+                    n = fs.numel()
+                    lo, hi = n * j // n_copy, n * (j + 1) // n_copy
+                    if hi > lo:
+                        fd[lo:hi].copy_(fs[lo:hi], non_blocking=True)
+            in_ready[b][j].record(cs)
 
-    for _ in range(2):
-        e2e_step()
+    def issue_compute(b):
+        for e_ in in_ready[b]:
+            stream.wait_event(e_)
+        stream.wait_event(out_done[b])            # y / counts of set b were copied out
+        bx, bidx, bw, beo = d_ins[b]
+        by, bcnt = d_outs[b]
+        r = moedc.moedc_layout(bidx, T, K, E, R, cap, bcnt, rk, inr, sl, ws, wsb, st, stream)
+        r |= moedc.moedc_dispatch(bx, T, H, bidx, sl, bcnt, K, E, cap, c.dtype, recv, scales, src,
+                                  st, stream)
+        r |= moedc.moedc_combine(beo, E, cap, H, bidx, sl, bw, T, K, by, st, stream)
+        if r != 0:
+            raise RuntimeError(f"libmoedc returned {r}")
+        comp_done[b].record(stream)
+
+    def issue_d2h(b):
+        back_stream.wait_event(comp_done[b])
+        with torch.cuda.stream(back_stream):
+            h_outs[b][0].copy_(d_outs[b][0], non_blocking=True)
+            h_outs[b][1].copy_(d_outs[b][1], non_blocking=True)
+        out_done[b].record(back_stream)
+
+    def run_e2e(n):
+        issue_h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                issue_h2d((i + 1) % 2)
+            issue_compute(i % 2)
+            issue_d2h(i % 2)
+
+    run_e2e(3)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    for cs in copy_streams + [back_stream]:
+        cs.wait_event(e0)
+    run_e2e(e2e_steps)
+    stream.wait_event(out_done[(e2e_steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_value = whole_job_gbs(step_bytes, world, e2e_ms)
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
+    # the pipelined path still returns this workload's y
+    if not torch.equal(h_outs[(e2e_steps - 1) % 2][0].view(torch.int16),
+                       d_outs[(e2e_steps - 1) % 2][0].cpu().view(torch.int16)):
+        raise RuntimeError("end-to-end result differs from the device result")
 
     side = None if args.no_side else side_workloads(dev)
     if rank != 0:
@@ -666,8 +719,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                     "steps": e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "path": "pinned host -> device copies of x, topk_idx, topk_weights, "
-                            "expert_out; moedc_layout, moedc_dispatch, moedc_combine; y and "
-                            "counts back to pinned host"},
+                            "expert_out (4 copy streams, two device input sets, the next "
+                            "step's copies overlapping this step's kernels); moedc_layout, "
+                            "moedc_dispatch, moedc_combine; y and counts back to pinned host "
+                            "on a third stream"},
             "gpu_launches": launches_per_step * K_steps,
             "kernel_timing": f"per-kernel durations from a second pass of {K_inst} steps with "
                              "events between kernels; the step time comes from the clean pass",
