@@ -42,6 +42,9 @@
  *    MOEDC_ERR_CAPACITY      an expert received more than cap entries; the
  *                            slots still count on, and the entries whose slot
  *                            is >= cap are dropped by dispatch and combine.
+ *  MOEDC_ERR_TIMEOUT is reserved: no kernel of this library waits on data
+ *  written by another block (the only wait is the hardware's
+ *  griddepcontrol.wait for the previous kernel of the stream).
  *
  * Sources (page title, part of the page):
  *  [UCCL749]  UCCL PR #749 "[EP] Low-latency mode batch tokens per

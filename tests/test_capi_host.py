@@ -145,3 +145,20 @@ def test_bench_max_over_ranks_gloo_two_processes():
     res = sorted(q.get(timeout=5) for _ in range(2))
     assert [r[1] for r in res] == [2.0, 2.0]            # both see the slowest rank
     assert all(abs(r[2] - 1000.0) < 1e-9 for r in res)  # 2 x 1 GB / 2 ms
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No CPU fallback: without the built library every call raises."""
+    with pytest.raises(RuntimeError, match="not found"):
+        moedc.load(str(tmp_path / "libmoedc.so"))
+
+
+def test_product_package_does_not_import_the_oracle():
+    import combine_moedc_layout_gb300 as pkg
+    pkg_dir = os.path.dirname(pkg.__file__)
+    for root, _, files in os.walk(pkg_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(root, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "moedc_oracle" not in src, f
