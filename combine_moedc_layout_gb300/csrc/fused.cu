@@ -7,18 +7,58 @@
 // notes: split by (token, slice) with a 512-element floor), and that a grid
 // barrier cost more than the copy it was meant to parallelise (relay note:
 // block-local barriers only).  So every block recomputes the tiny layout in
-// shared memory, block 0 alone publishes it, and all blocks copy slices.
+// shared memory and copies slices; nothing waits on another block.
+//
+// The block's latency chain is what the launch costs, so each step is kept
+// short: the first x slice and all routing ids are loaded up front (one DRAM
+// round trip for both), per-warp expert counts come from shared-memory
+// atomics, the in-tile ranking uses a bit-sliced ballot match (eleven
+// independent ballots; the hardware match instruction was measured several
+// times slower here), and the layout outputs are written by the warps that
+// touch them (a token's slots by the warp copying its first slice, each
+// rank's distinct-token count by one warp of the grid) instead of by one
+// block after the others have finished their copies.
 #include <climits>
+#include <mutex>
 
 #include "dispatch_item.cuh"
 
 namespace moedc {
 
-constexpr int kFusedThreads = 128;
-constexpr int kFusedWarps = kFusedThreads / kWarp;
+// Block width follows the entry count: every thread holds two routing ids,
+// so 128-thread blocks take up to 256 entries and 512-thread blocks the rest.
+// Narrow blocks keep more SMs copying when there are few tokens; wide blocks
+// shorten each warp's share of the layout when there are many (measured: at 4
+// tokens 128 threads beat 512 by 3 us, at 1024 entries 512 beat 128 by 2 us).
+constexpr int kFusedIdsPerThread = 2;
+constexpr int kFusedNarrow = 128;
+constexpr int kFusedWide = MOEDC_FUSED_MAX_ENTRIES / kFusedIdsPerThread;
+static_assert(kFusedWide == 512, "wide fused block");
+constexpr int kKeyBits = 11;   // keys are expert + 1 <= MOEDC_MAX_E
+static_assert(MOEDC_MAX_E < (1 << kKeyBits), "ballot match key width");
 
-template <bool kFp8, bool kScaleCols>
-__global__ void __launch_bounds__(kFusedThreads)
+// Lanes of the warp holding the same key (0 <= key < 2^kKeyBits): the
+// intersection, over the key's bits, of the lanes that agree on that bit.
+__device__ __forceinline__ unsigned match_key(int key)
+{
+    unsigned peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < kKeyBits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const unsigned m = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// Shared memory (int32 words) of one block of `threads` for n entries, E experts.
+__host__ __device__ constexpr size_t fused_smem_words(int threads, int n, int E)
+{
+    return 2 * (size_t)n + (size_t)(threads / kWarp + 1) * E;
+}
+
+template <int kThreads, bool kFp8, bool kScaleCols>
+__global__ void __launch_bounds__(kThreads)
 fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
                              int T, int H, int K, int E, int R, int cap,
                              int32_t* __restrict__ num_tokens_per_expert,
@@ -27,39 +67,57 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
                              void* __restrict__ recv, float* __restrict__ scales,
                              int32_t* __restrict__ src_idx, int32_t* __restrict__ status)
 {
+    constexpr int kFusedWarps = kThreads / kWarp;
     pdl_enter();
     extern __shared__ int32_t smem[];
-    const int n = T * K;
+    const int n = T * K;                        // <= kThreads * kFusedIdsPerThread
     int32_t* s_idx = smem;                      // [n]
     int32_t* s_slot = s_idx + n;                // [n]
     int32_t* s_wcnt = s_slot + n;               // [kFusedWarps][E] per-warp counts, then offsets
-    int32_t* s_cnt = s_wcnt + kFusedWarps * E;  // [E] totals, then block 0's [R] rank counts
+    int32_t* s_cnt = s_wcnt + kFusedWarps * E;  // [E] totals
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int epr = E / R;
+    const int nslice = (H + kSlice - 1) / kSlice;
+    const int items = T * nslice;
+    const int nwarps = gridDim.x * kFusedWarps;
 
-    for (int i = threadIdx.x; i < kFusedWarps * E; i += blockDim.x) s_wcnt[i] = 0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s_idx[i] = topk_idx[i];
+    // the warp's first x slice does not depend on the layout: start it now
+    int item = blockIdx.x * kFusedWarps + warp;
+    SliceX xv{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (item < items) {
+        const int t = item / nslice;
+        xv = load_slice<kFp8>(x + (int64_t)t * H, H, item - t * nslice, lane);
+    }
+    {
+        int v[kFusedIdsPerThread];
+#pragma unroll
+        for (int j = 0; j < kFusedIdsPerThread; ++j) {
+            const int i = threadIdx.x + j * kThreads;
+            v[j] = i < n ? topk_idx[i] : 0;
+        }
+        for (int i = threadIdx.x; i < kFusedWarps * E; i += kThreads) s_wcnt[i] = 0;
+#pragma unroll
+        for (int j = 0; j < kFusedIdsPerThread; ++j) {
+            const int i = threadIdx.x + j * kThreads;
+            if (i < n) s_idx[i] = v[j];
+        }
+    }
     __syncthreads();
 
-    // layout: each warp takes a contiguous run of 32-entry tiles in (t, k)
-    // order, counts it per expert, the counts are scanned across warps, then
-    // each warp ranks equal experts inside its tiles with __match_any_sync
+    // layout: each warp owns a contiguous run of 32-entry tiles in (t, k)
+    // order; count the run per expert, scan the counts across warps, then
+    // rank equal experts inside each tile in lane order
     const int run = ((n + kFusedWarps * kWarp - 1) / (kFusedWarps * kWarp)) * kWarp;
     const int wbeg = min(n, warp * run);
     const int wend = min(n, wbeg + run);
     int32_t* my = s_wcnt + warp * E;
-    const unsigned lt = lanemask_lt();
-    for (int i0 = wbeg; i0 < wend; i0 += kWarp) {
-        const int i = i0 + lane;
-        const int e = i < wend ? s_idx[i] : -1;
-        const bool v = e >= 0 && e < E;
-        const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1);
-        if (v && (peers & lt) == 0) my[e] += __popc(peers);
-        __syncwarp();
+    for (int i = wbeg + lane; i < wend; i += kWarp) {
+        const int e = s_idx[i];
+        if (e >= 0 && e < E) atomicAdd(&my[e], 1);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    for (int e = threadIdx.x; e < E; e += kThreads) {
         int acc = 0;
 #pragma unroll
         for (int w = 0; w < kFusedWarps; ++w) {
@@ -70,11 +128,12 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
         s_cnt[e] = acc;
     }
     __syncthreads();
+    const unsigned lt = lanemask_lt();
     for (int i0 = wbeg; i0 < wend; i0 += kWarp) {
         const int i = i0 + lane;
         const int e = i < wend ? s_idx[i] : -1;
         const bool v = e >= 0 && e < E;
-        const unsigned peers = __match_any_sync(0xffffffffu, v ? e : -1);
+        const unsigned peers = match_key(v ? e + 1 : 0);
         int sv = -1;
         if (v) sv = my[e] + __popc(peers & lt);
         __syncwarp();
@@ -85,65 +144,102 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
     __syncthreads();
 
     if (blockIdx.x == 0) {
-        // block 0 publishes the layout; rank membership is a range test per
-        // (token, rank) pair, spread over all threads, counted in shared memory
-        int32_t* s_rank = s_cnt + E;   // [R] (after the totals)
-        for (int r = threadIdx.x; r < R; r += blockDim.x) s_rank[r] = 0;
-        bool bad = false;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            slot[i] = s_slot[i];
-            const int e = s_idx[i];
-            if (e < -1 || e >= E) bad = true;
-        }
-        if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        for (int e = threadIdx.x; e < E; e += kThreads) {
             num_tokens_per_expert[e] = s_cnt[e];
             if (s_cnt[e] > cap) raise_status(status, MOEDC_ERR_CAPACITY);
         }
-        __syncthreads();   // s_rank zeroed
-        for (int b = threadIdx.x; b < T * R; b += blockDim.x) {
-            const int t = b / R;
-            const int r = b - t * R;
-            const unsigned lo = (unsigned)(r * epr);
-            uint8_t flag = 0;
-            for (int k = 0; k < K; ++k)
-                flag |= ((unsigned)s_idx[t * K + k] - lo < (unsigned)epr) ? 1 : 0;
-            is_token_in_rank[b] = flag;
-            if (flag) atomicAdd(&s_rank[r], 1);
+    }
+    // distinct tokens per rank: one warp of the grid per rank
+    for (int r = blockIdx.x * kFusedWarps + warp; r < R; r += nwarps) {
+        const unsigned lo = (unsigned)(r * epr);
+        int c = 0;
+        for (int t = lane; t < T; t += kWarp) {
+            bool f = false;
+            for (int k = 0; k < K; ++k) f |= (unsigned)s_idx[t * K + k] - lo < (unsigned)epr;
+            c += f;
         }
-        __syncthreads();
-        for (int r = threadIdx.x; r < R; r += blockDim.x) num_tokens_per_rank[r] = s_rank[r];
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) num_tokens_per_rank[r] = c;
     }
 
     // src_idx: -1 past each expert's count (grid-strided), t for filled slots
     {
         const int64_t total = (int64_t)E * cap;
-        const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += nthreads) {
+        const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+        for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
+             i += nthreads) {
             const int e = (int)(i / cap);
             const int s = (int)(i - (int64_t)e * cap);
             if (s >= s_cnt[e]) src_idx[i] = -1;
         }
     }
 
-    const int nslice = (H + kSlice - 1) / kSlice;
-    const int items = T * nslice;
-    const int nwarps = gridDim.x * kFusedWarps;
-    for (int item = blockIdx.x * kFusedWarps + warp; item < items; item += nwarps) {
+    for (; item < items; item += nwarps) {
         const int t = item / nslice;
         const int sl = item - t * nslice;
         int my_row = -1;
         if (lane < K) {
-            my_row = dest_row(s_idx[t * K + lane], s_slot[t * K + lane], E, cap);
-            if (sl == 0 && my_row >= 0) src_idx[my_row] = t;
+            const int e = s_idx[t * K + lane];
+            const int sv = s_slot[t * K + lane];
+            my_row = dest_row(e, sv, E, cap);
+            if (sl == 0) {   // the warp copying a token's first slice publishes its entries
+                slot[t * K + lane] = sv;
+                if (e < -1 || e >= E) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+                if (my_row >= 0) src_idx[my_row] = t;
+            }
         }
-        const SliceX v = load_slice<kFp8>(x + (int64_t)t * H, H, sl, lane);
+        if (sl == 0) {
+            for (int r = lane; r < R; r += kWarp) {
+                const unsigned lo = (unsigned)(r * epr);
+                uint8_t flag = 0;
+                for (int k = 0; k < K; ++k)
+                    flag |= ((unsigned)s_idx[t * K + k] - lo < (unsigned)epr) ? 1 : 0;
+                is_token_in_rank[(int64_t)t * R + r] = flag;
+            }
+        }
         const int64_t sbase = kScaleCols ? colmajor_scale_base(my_row, cap, H / 128) : 0;
-        store_slice<kFp8, kScaleCols>(v, H, sl, lane, K, my_row, recv, scales, sbase, cap);
+        store_slice<kFp8, kScaleCols>(xv, H, sl, lane, K, my_row, recv, scales, sbase, cap);
+        const int next = item + nwarps;
+        if (next < items) {
+            const int t2 = next / nslice;
+            xv = load_slice<kFp8>(x + (int64_t)t2 * H, H, next - t2 * nslice, lane);
+        }
     }
 }
 
 }  // namespace moedc
+
+namespace {
+
+// The wide block at its largest (1024 entries, MOEDC_MAX_E experts) needs
+// more than the default 48 KB of dynamic shared memory: raise the limit of
+// its three instances once.  The attribute is per function and per device.
+// (The narrow block needs at most 2 * 256 + 5 * MOEDC_MAX_E words, 22.5 KB.)
+constexpr int kMaxDevices = 64;
+std::mutex g_smem_mutex;
+bool g_smem_set[kMaxDevices] = {};
+
+bool fused_smem_ready()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    if (g_smem_set[dev]) return true;
+    constexpr int W = moedc::kFusedWide;
+    const int bytes = (int)(moedc::fused_smem_words(W, MOEDC_FUSED_MAX_ENTRIES, MOEDC_MAX_E) *
+                            sizeof(int32_t));
+    if (cudaFuncSetAttribute(moedc::fused_layout_dispatch_kernel<W, false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(moedc::fused_layout_dispatch_kernel<W, true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(moedc::fused_layout_dispatch_kernel<W, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    g_smem_set[dev] = true;
+    return true;
+}
+
+}  // namespace
 
 extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int T, int H, int K,
                                      int E, int R, int cap, int out_dtype,
@@ -187,28 +283,47 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
 
     const int nslice = (H + moedc::kSlice - 1) / moedc::kSlice;
     const int64_t items = (int64_t)T * nslice;
-    int64_t blocks = (items + moedc::kFusedWarps - 1) / moedc::kFusedWarps;
-    const int64_t fill_blocks = ((int64_t)E * cap + moedc::kFusedThreads - 1) / moedc::kFusedThreads;
+    const bool wide = n > (int64_t)moedc::kFusedNarrow * moedc::kFusedIdsPerThread;
+    const int threads = wide ? moedc::kFusedWide : moedc::kFusedNarrow;
+    int64_t blocks = (items + threads / moedc::kWarp - 1) / (threads / moedc::kWarp);
+    const int64_t fill_blocks = ((int64_t)E * cap + threads - 1) / threads;
     if (blocks < fill_blocks) blocks = fill_blocks;
-    const void* fn = base == MOEDC_BF16
-                         ? (const void*)moedc::fused_layout_dispatch_kernel<false, false>
-                     : cols ? (const void*)moedc::fused_layout_dispatch_kernel<true, true>
-                            : (const void*)moedc::fused_layout_dispatch_kernel<true, false>;
-    const size_t sm = (size_t)(2 * n + (moedc::kFusedWarps + 1) * E + R) * sizeof(int32_t);
-    const int64_t resident = resident_blocks(fn, moedc::kFusedThreads, sm);
+    const void* fn;
+    if (wide) {
+        constexpr int W = moedc::kFusedWide;
+        fn = base == MOEDC_BF16 ? (const void*)moedc::fused_layout_dispatch_kernel<W, false, false>
+             : cols             ? (const void*)moedc::fused_layout_dispatch_kernel<W, true, true>
+                                : (const void*)moedc::fused_layout_dispatch_kernel<W, true, false>;
+        if (!fused_smem_ready()) return MOEDC_ERR_CUDA;
+    } else {
+        constexpr int N = moedc::kFusedNarrow;
+        fn = base == MOEDC_BF16 ? (const void*)moedc::fused_layout_dispatch_kernel<N, false, false>
+             : cols             ? (const void*)moedc::fused_layout_dispatch_kernel<N, true, true>
+                                : (const void*)moedc::fused_layout_dispatch_kernel<N, true, false>;
+    }
+    const size_t sm = moedc::fused_smem_words(threads, (int)n, E) * sizeof(int32_t);
+    const int64_t resident = resident_blocks(fn, threads, sm);
     if (blocks > resident) blocks = resident;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     clear_stale_error();
-#define MOEDC_FUSED_LAUNCH(F, C)                                                                 \
-    launch(moedc::fused_layout_dispatch_kernel<F, C>, (int)blocks, moedc::kFusedThreads, sm, stream, \
-        xb, topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,          \
-        is_token_in_rank, slot, recv, scales, src_idx, dev_status)
-    if (base == MOEDC_BF16)
-        MOEDC_FUSED_LAUNCH(false, false);
-    else if (cols)
-        MOEDC_FUSED_LAUNCH(true, true);
+#define MOEDC_FUSED_LAUNCH(NT, F, C)                                                             \
+    launch(moedc::fused_layout_dispatch_kernel<NT, F, C>, (int)blocks, NT, sm, stream, xb,       \
+           topk_idx, T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,            \
+           is_token_in_rank, slot, recv, scales, src_idx, dev_status)
+#define MOEDC_FUSED_DTYPE(NT)                                                                    \
+    do {                                                                                         \
+        if (base == MOEDC_BF16)                                                                  \
+            MOEDC_FUSED_LAUNCH(NT, false, false);                                                \
+        else if (cols)                                                                           \
+            MOEDC_FUSED_LAUNCH(NT, true, true);                                                  \
+        else                                                                                     \
+            MOEDC_FUSED_LAUNCH(NT, true, false);                                                 \
+    } while (0)
+    if (wide)
+        MOEDC_FUSED_DTYPE(moedc::kFusedWide);
     else
-        MOEDC_FUSED_LAUNCH(true, false);
+        MOEDC_FUSED_DTYPE(moedc::kFusedNarrow);
+#undef MOEDC_FUSED_DTYPE
 #undef MOEDC_FUSED_LAUNCH
     return launch_status();
 }

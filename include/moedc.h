@@ -272,8 +272,10 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * [MORI614 notes on low token counts: host enqueue and idle warps dominate].
  * For T * K <= MOEDC_FUSED_MAX_ENTRIES this is ONE kernel launch: every
  * thread block rebuilds the layout in shared memory (no inter-block
- * synchronisation), block 0 writes the layout outputs, and all blocks split
- * the (token, 512-channel slice) copies.  Larger inputs run moedc_layout and
+ * synchronisation), the blocks split the (token, 512-channel slice) copies,
+ * and each layout output is written by the warp that owns it (a token's slots
+ * and rank flags by the warp copying its first slice, a rank's count by one
+ * warp, the expert counts by block 0).  Larger inputs run moedc_layout and
  * moedc_dispatch back to back.  Results are identical either way.
  * workspace: as for moedc_layout (never used on the single-launch path).
  */

@@ -48,6 +48,18 @@ RANDOM = {
                         scale=1e30),
     "large_t": dict(seed=22, T=40000, H=128, K=8, E=128, R=8, cap=None, dtype=synth.BF16,
                     mask_p=0.01),
+    # single-launch layout+dispatch: both block widths, the width boundary
+    # (256 entries narrow, 257 wide), the largest shared-memory block (1024
+    # entries, 1024 experts) and more ranks than the grid has warps
+    "fused_n256": dict(seed=23, T=32, H=1024, K=8, E=64, R=8, cap=None, dtype=synth.FP8_E4M3,
+                       mask_p=0.1),
+    "fused_n257": dict(seed=24, T=257, H=640, K=1, E=16, R=4, cap=None, dtype=synth.BF16),
+    "fused_n264_dup": dict(seed=25, T=33, H=1536, K=8, E=12, R=3, cap=None,
+                           dtype=synth.FP8_E4M3, distinct=False, mask_p=0.05),
+    "fused_max_e": dict(seed=26, T=128, H=256, K=8, E=1024, R=8, cap=None,
+                        dtype=synth.FP8_E4M3),
+    "fused_many_ranks": dict(seed=27, T=100, H=128, K=10, E=512, R=512, cap=None,
+                             dtype=synth.BF16, mask_p=0.02),
 }
 
 
@@ -91,7 +103,8 @@ def test_parity(key):
 @pytest.mark.parametrize("key", [pytest.param(n, id=n) for n in
                                  ["tiny", "low4", "low8", "low16", "default_ll"]] +
                          [pytest.param("r:" + k, id=k) for k in
-                          ["k1", "e_eq_r", "t1", "h8", "duplicates"]])
+                          ["k1", "e_eq_r", "t1", "h8", "duplicates", "fused_n256", "fused_n257",
+                           "fused_n264_dup", "fused_max_e", "fused_many_ranks"]])
 def test_fused_layout_dispatch_matches_oracle(key):
     c = get_case(key)
     d = DevCase(c)
