@@ -63,6 +63,8 @@ def _load():
     lib.oracle_e4m3_decode_n.argtypes = [P, P, I64]
     lib.oracle_f32_to_bf16_n.argtypes = [P, P, I64]
     lib.oracle_dequant_e4m3.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_dequant_e4m3_token.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_dispatch_token_scale.argtypes = [P, I, I, P, P, I, I, I, P, P, P]
     lib.oracle_rank_layout.argtypes = [P, I, I, I, P]
     lib.oracle_rank_layout.restype = I
     lib.oracle_rank_dispatch.argtypes = [P, I, I, P, I, I, I, P, P, P]
@@ -139,6 +141,26 @@ def dispatch(x: np.ndarray, topk_idx: np.ndarray, slot: np.ndarray, E: int, cap:
     return dict(recv=recv, scales=scales if fp8 else None, src_idx=src_idx, status=status)
 
 
+def dispatch_token_scale(x: np.ndarray, topk_idx: np.ndarray, slot: np.ndarray, E: int,
+                         cap: int, recv: np.ndarray | None = None) -> dict:
+    """e4m3 dispatch with one scale per token row.  Returns recv (uint8
+    [E,cap,H]), scales (float32 [E,cap]), src_idx and status; untouched rows
+    keep their initial contents (zeros unless `recv` is given)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    T, H = x.shape
+    K = topk_idx.shape[1] if topk_idx.ndim == 2 else 0
+    if recv is None:
+        recv = np.zeros((E, cap, H), np.uint8)
+    scales = np.zeros((E, cap), np.float32)
+    src_idx = np.empty((E, cap), np.int32)
+    status = _load().oracle_dispatch_token_scale(_ptr(x), T, H, _ptr(topk_idx), _ptr(slot), K,
+                                                 E, cap, _ptr(recv), _ptr(scales),
+                                                 _ptr(src_idx))
+    return dict(recv=recv, scales=scales, src_idx=src_idx, status=status)
+
+
 def combine(expert_out: np.ndarray, topk_idx: np.ndarray, slot: np.ndarray,
             topk_weights: np.ndarray) -> dict:
     """expert_out: uint16 bf16 bits [E, cap, H].  Returns y (uint16 [T, H]) and status."""
@@ -166,6 +188,19 @@ def dequant_e4m3(recv: np.ndarray, scales: np.ndarray, num_tokens_per_expert: np
     if out is None:
         out = np.zeros((E, cap, H), np.uint16)
     _load().oracle_dequant_e4m3(_ptr(recv), _ptr(scales), _ptr(cnt), E, cap, H, _ptr(out))
+    return out
+
+
+def dequant_e4m3_token(recv: np.ndarray, scales: np.ndarray, num_tokens_per_expert: np.ndarray,
+                       out: np.ndarray | None = None) -> np.ndarray:
+    """As dequant_e4m3 with one scale per row: scales float32 [E, cap]."""
+    recv = np.ascontiguousarray(recv, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    cnt = np.ascontiguousarray(num_tokens_per_expert, dtype=np.int32)
+    E, cap, H = recv.shape
+    if out is None:
+        out = np.zeros((E, cap, H), np.uint16)
+    _load().oracle_dequant_e4m3_token(_ptr(recv), _ptr(scales), _ptr(cnt), E, cap, H, _ptr(out))
     return out
 
 
@@ -205,9 +240,11 @@ def rank_combine(rank_out: np.ndarray, rank_slot: np.ndarray) -> np.ndarray:
 
 
 def combine_e4m3(expert_out: np.ndarray, expert_scales: np.ndarray, topk_idx: np.ndarray,
-                 slot: np.ndarray, topk_weights: np.ndarray, scale_cols: bool = False) -> dict:
+                 slot: np.ndarray, topk_weights: np.ndarray, scale_cols: bool = False,
+                 per_token: bool = False) -> dict:
     """expert_out: e4m3 codes uint8 [E, cap, H]; expert_scales float32 [E, cap, H/128]
-    (or [E, H/128, cap] with scale_cols).  Returns y (bf16 bits [T, H]) and status."""
+    (or [E, H/128, cap] with scale_cols, or [E, cap] with per_token).  Returns
+    y (bf16 bits [T, H]) and status."""
     expert_out = np.ascontiguousarray(expert_out, dtype=np.uint8)
     expert_scales = np.ascontiguousarray(expert_scales, dtype=np.float32)
     topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
@@ -217,6 +254,7 @@ def combine_e4m3(expert_out: np.ndarray, expert_scales: np.ndarray, topk_idx: np
     T, K = topk_idx.shape
     y = np.empty((T, H), np.uint16)
     status = _load().oracle_combine_e4m3(_ptr(expert_out), _ptr(expert_scales),
-                                         1 if scale_cols else 0, E, cap, H, _ptr(topk_idx),
+                                         2 if per_token else 1 if scale_cols else 0, E, cap,
+                                         H, _ptr(topk_idx),
                                          _ptr(slot), _ptr(topk_weights), T, K, _ptr(y))
     return dict(y=y, status=status)

@@ -265,6 +265,51 @@ int oracle_dispatch(const uint16_t* x, int T, int H, const int32_t* topk_idx,
     return status;
 }
 
+/*
+ * Dispatch with one e4m3 scale per token row.  The rule is the per-128
+ * rule above with the group widened to the whole row of H channels:
+ *   a = max_h |x[t][h]|                      (exact)
+ *   a = fmaxf(a, 1e-4f)
+ *   s = a / 448.0f                             (one IEEE binary32 division)
+ *   recv[e][s][h] = e4m3(x[t][h] / s)          (binary32 division, then the
+ *                                               satfinite nearest-even encode)
+ *   scales[e][s] = s                           (scales is [E][cap])
+ * src_idx and the untouched rows as in oracle_dispatch.
+ */
+int oracle_dispatch_token_scale(const uint16_t* x, int T, int H, const int32_t* topk_idx,
+                                const int32_t* slot, int K, int E, int cap,
+                                uint8_t* recv, float* scales, int32_t* src_idx)
+{
+    int status = ORACLE_OK;
+    for (int64_t i = 0; i < (int64_t)E * cap; ++i)
+        src_idx[i] = -1;
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* xr = x + (int64_t)t * H;
+        float amax = 0.0f;
+        for (int h = 0; h < H; ++h) {
+            float v = fabsf(oracle_bf16_to_f32(xr[h]));
+            if (v > amax)
+                amax = v;
+        }
+        amax = fmaxf(amax, 1e-4f);
+        float scale = amax / 448.0f;
+        for (int k = 0; k < K; ++k) {
+            int e = topk_idx[(int64_t)t * K + k];
+            int s = slot[(int64_t)t * K + k];
+            if (e < -1 || e >= E)
+                status = raise_status(status, ORACLE_ERR_EXPERT_RANGE);
+            if (!entry_valid(e, s, E, cap))
+                continue;
+            int64_t row = (int64_t)e * cap + s;
+            src_idx[row] = t;
+            for (int h = 0; h < H; ++h)
+                recv[row * H + h] = oracle_e4m3_encode(oracle_bf16_to_f32(xr[h]) / scale);
+            scales[row] = scale;
+        }
+    }
+    return status;
+}
+
 /* -------------------------------------------------------------- combine */
 /*
  * Combine.  For every token t and channel h:
@@ -325,6 +370,23 @@ void oracle_dequant_e4m3(const uint8_t* recv, const float* scales,
             for (int h = 0; h < H; ++h) {
                 float v = oracle_e4m3_decode(recv[row * H + h]);
                 float p = v * scales[row * G + h / 128];
+                out[row * H + h] = oracle_f32_to_bf16(p);
+            }
+        }
+    }
+}
+
+/* the same with one scale per row (scales [E][cap]): p = decode(q) * scales[e][s] */
+void oracle_dequant_e4m3_token(const uint8_t* recv, const float* scales,
+                               const int32_t* num_tokens_per_expert, int E, int cap, int H,
+                               uint16_t* out)
+{
+    for (int e = 0; e < E; ++e) {
+        int filled = num_tokens_per_expert[e] < cap ? num_tokens_per_expert[e] : cap;
+        for (int s = 0; s < filled; ++s) {
+            int64_t row = (int64_t)e * cap + s;
+            for (int h = 0; h < H; ++h) {
+                float p = oracle_e4m3_decode(recv[row * H + h]) * scales[row];
                 out[row * H + h] = oracle_f32_to_bf16(p);
             }
         }
@@ -439,8 +501,9 @@ void oracle_rank_combine(const uint16_t* rank_out, int R, int cap_rank, int H,
 
 /* -------------------------------------------------------- e4m3 combine */
 /*
- * Combine from e4m3 expert outputs with per-128-channel fp32 scales
- * (expert_scales row-major [E][cap][G], or [E][G][cap] when scale_cols != 0).
+ * Combine from e4m3 expert outputs with fp32 scales.  scale_mode 0: one scale
+ * per 128 channels, row-major [E][cap][G]; 1: the same column-major
+ * [E][G][cap]; 2: one scale per row, [E][cap].
  * For every token t and channel h, group g = h / 128:
  *   acc = 0.0f
  *   for k = 0 .. K-1 ascending, skipping masked / out-of-range / dropped entries:
@@ -449,7 +512,7 @@ void oracle_rank_combine(const uint16_t* rank_out, int R, int cap_rank, int H,
  *       acc = acc + p                                (binary32 add)
  *   y[t][h] = bf16(acc), nearest even.
  */
-int oracle_combine_e4m3(const uint8_t* expert_out, const float* expert_scales, int scale_cols,
+int oracle_combine_e4m3(const uint8_t* expert_out, const float* expert_scales, int scale_mode,
                         int E, int cap, int H, const int32_t* topk_idx, const int32_t* slot,
                         const float* topk_weights, int T, int K, uint16_t* y)
 {
@@ -470,8 +533,9 @@ int oracle_combine_e4m3(const uint8_t* expert_out, const float* expert_scales, i
                 if (!entry_valid(e, s, E, cap))
                     continue;
                 int64_t row = (int64_t)e * cap + s;
-                float sc = scale_cols ? expert_scales[((int64_t)e * G + g) * cap + s]
-                                      : expert_scales[row * G + g];
+                float sc = scale_mode == 2   ? expert_scales[row]
+                           : scale_mode == 1 ? expert_scales[((int64_t)e * G + g) * cap + s]
+                                             : expert_scales[row * G + g];
                 float v = oracle_e4m3_decode(expert_out[row * H + h]) * sc;
                 float p = topk_weights[(int64_t)t * K + k] * v;
                 acc = acc + p;
