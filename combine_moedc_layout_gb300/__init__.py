@@ -4,7 +4,7 @@ The compute runs in the CUDA library libmoedc.so (built by build.build());
 this package holds its ctypes binding (moedc) and the seeded synthetic
 workloads (synth).
 """
-from .moedc import (BF16, FP8_E4M3, SCALES_COL_MAJOR, Layout, MoedcError, alloc_recv, combine,
+from .moedc import (BF16, FP8_E4M3, SCALES_COL_MAJOR, SCALES_PER_TOKEN, Layout, MoedcError, alloc_recv, combine,
                     combine_e4m3, dequant_e4m3, moedc_combine_e4m3,
                     dispatch, layout, layout_dispatch, layout_workspace, load, moedc_combine,
                     moedc_dequant_e4m3, moedc_dispatch, moedc_layout, moedc_layout_dispatch,
@@ -12,7 +12,7 @@ from .moedc import (BF16, FP8_E4M3, SCALES_COL_MAJOR, Layout, MoedcError, alloc_
                     moedc_rank_combine, moedc_rank_dispatch, moedc_rank_layout, rank_combine,
                     rank_dispatch, rank_layout, strerror)
 
-__all__ = ["BF16", "FP8_E4M3", "SCALES_COL_MAJOR", "Layout", "MoedcError", "alloc_recv",
+__all__ = ["BF16", "FP8_E4M3", "SCALES_COL_MAJOR", "SCALES_PER_TOKEN", "Layout", "MoedcError", "alloc_recv",
            "combine", "combine_e4m3", "dequant_e4m3", "moedc_combine_e4m3",
            "dispatch", "layout", "layout_dispatch", "layout_workspace", "load", "moedc_combine",
            "moedc_dequant_e4m3", "moedc_dispatch", "moedc_layout", "moedc_layout_dispatch",

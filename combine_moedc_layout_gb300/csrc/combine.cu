@@ -168,7 +168,7 @@ constexpr int kCombine8Batch = 8;
 // (one 16-byte load of codes per row, all in one 128-channel scale group).
 __global__ void __launch_bounds__(kCombineThreads, 2)
 combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restrict__ scales,
-                    bool scale_cols, int E, int cap, int H, const int32_t* __restrict__ topk_idx,
+                    int scale_mode, int E, int cap, int H, const int32_t* __restrict__ topk_idx,
                     const int32_t* __restrict__ slot, const float* __restrict__ topk_weights,
                     int T, int K, uint16_t* __restrict__ y, int32_t* __restrict__ status)
 {
@@ -209,9 +209,10 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
                 wk[j] = __shfl_sync(0xffffffffu, my_w, k & 31);
                 ok[j] = k < K && e >= 0 && e < E && s >= 0 && s < cap;
                 const int64_t row = ok[j] ? (int64_t)e * cap + s : 0;
-                const int64_t si = !ok[j] ? 0
-                                   : scale_cols ? ((int64_t)e * G + g) * cap + s
-                                                : row * G + g;
+                const int64_t si = !ok[j]           ? 0
+                                   : scale_mode == 2 ? row                              // per row
+                                   : scale_mode == 1 ? ((int64_t)e * G + g) * cap + s   // [E][G][cap]
+                                                     : row * G + g;                     // [E][cap][G]
                 q[j] = ld_global_nc(reinterpret_cast<const uint4*>(expert_out + row * H +
                                                                      (act ? c0 : 0)));
                 sc[j] = __ldg(scales + si);
@@ -260,7 +261,8 @@ extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_sc
                                   int32_t* dev_status, cudaStream_t stream)
 {
     using namespace moedc_host;
-    if (scale_layout != 0 && scale_layout != MOEDC_SCALES_COL_MAJOR) return MOEDC_ERR_ARG;
+    const int mode = scale_mode(scale_layout);
+    if (mode < 0) return MOEDC_ERR_ARG;
     if (T < 0 || H < 128 || H % 128 != 0 || K < 1 || K > MOEDC_MAX_K || E < 1 ||
         E > MOEDC_MAX_E || cap < 1)
         return MOEDC_ERR_ARG;
@@ -280,7 +282,7 @@ extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_sc
         resident_blocks((const void*)moedc::combine_e4m3_kernel, moedc::kCombineThreads, 0);
     if (blocks > resident) blocks = resident;
     clear_stale_error();
-    launch(moedc::combine_e4m3_kernel, (int)blocks, moedc::kCombineThreads, 0, stream, static_cast<const uint8_t*>(expert_out), expert_scales, scale_layout != 0, E, cap, H,
+    launch(moedc::combine_e4m3_kernel, (int)blocks, moedc::kCombineThreads, 0, stream, static_cast<const uint8_t*>(expert_out), expert_scales, mode, E, cap, H,
         topk_idx, slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status);
     return launch_status();
 }

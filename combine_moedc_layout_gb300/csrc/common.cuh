@@ -112,7 +112,20 @@ namespace moedc_host {
 // out_dtype: MOEDC_BF16, MOEDC_FP8_E4M3, or MOEDC_FP8_E4M3 | MOEDC_SCALES_COL_MAJOR
 inline bool dtype_ok(int d)
 {
-    return d == MOEDC_BF16 || d == MOEDC_FP8_E4M3 || d == (MOEDC_FP8_E4M3 | MOEDC_SCALES_COL_MAJOR);
+    return d == MOEDC_BF16 || d == MOEDC_FP8_E4M3 ||
+           d == (MOEDC_FP8_E4M3 | MOEDC_SCALES_COL_MAJOR) ||
+           d == (MOEDC_FP8_E4M3 | MOEDC_SCALES_PER_TOKEN);
+}
+// the element type of an out_dtype, without its scale-layout flag
+inline int dtype_base(int d) { return d & ~(MOEDC_SCALES_COL_MAJOR | MOEDC_SCALES_PER_TOKEN); }
+// scale index mode of a scale_layout argument: 0 rows [E][cap][G], 1 columns
+// [E][G][cap], 2 one per row [E][cap]; -1 for anything else
+inline int scale_mode(int layout)
+{
+    return layout == 0                        ? 0
+           : layout == MOEDC_SCALES_COL_MAJOR ? 1
+           : layout == MOEDC_SCALES_PER_TOKEN ? 2
+                                              : -1;
 }
 int sm_count();                 // multiprocessors of the current device
 // blocks of `kernel` resident on the whole current device at once
@@ -164,5 +177,10 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
                     const int32_t* num_tokens_per_expert, int K, int E, int cap, int out_dtype,
                     void* recv, float* scales, int32_t* src_idx, int32_t* dev_status,
                     cudaStream_t stream);
+// e4m3 dispatch with one scale per token row (dispatch_token.cu)
+int launch_dispatch_token(const void* x, int T, int H, const int32_t* topk_idx,
+                          const int32_t* slot, const int32_t* num_tokens_per_expert, int K,
+                          int E, int cap, void* recv, float* scales, int32_t* src_idx,
+                          int32_t* dev_status, cudaStream_t stream);
 
 }  // namespace moedc_host

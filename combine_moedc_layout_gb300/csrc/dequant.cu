@@ -1,5 +1,5 @@
-// e4m3 receive rows back to bf16: out = bf16(decode(q) * scale), per 128-channel
-// group scale.  This is the identity "expert" of a dispatch -> expert ->
+// e4m3 receive rows back to bf16: out = bf16(decode(q) * scale), with the
+// scale of the element's 128-channel group or of its whole row.  This is the identity "expert" of a dispatch -> expert ->
 // combine round (the dequantisation q * s that pairs with the e4m3 dispatch),
 // and the bf16 view an expert without an FP8 path would read.  Only the
 // filled rows (s < min(count, cap)) are converted.
@@ -17,7 +17,7 @@ constexpr int kDequantSlice = 512;   // channels per warp item (16 per lane)
 // memory, then a flat filled-row index f maps to its expert by binary search.
 __global__ void __launch_bounds__(kDequantThreads)
 dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ scales,
-                    bool scale_cols, const int32_t* __restrict__ num_tokens_per_expert, int E,
+                    int scale_mode, const int32_t* __restrict__ num_tokens_per_expert, int E,
                     int cap, int H, uint16_t* __restrict__ out)
 {
     pdl_enter();
@@ -79,8 +79,10 @@ dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ 
         if (c0 >= H) continue;
         const uint4 q = ld_global_nc(reinterpret_cast<const uint4*>(recv + row * H + c0));
         const int g = c0 / 128;
-        const float sc = __ldg(scales + (scale_cols ? ((int64_t)lo * G + g) * cap + sidx
-                                                    : row * G + g));
+        const int64_t si = scale_mode == 2   ? row                                   // per row
+                           : scale_mode == 1 ? ((int64_t)lo * G + g) * cap + sidx    // [E][G][cap]
+                                             : row * G + g;                          // [E][cap][G]
+        const float sc = __ldg(scales + si);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
 #pragma unroll
@@ -104,7 +106,8 @@ extern "C" int moedc_dequant_e4m3(const void* recv, const float* scales, int sca
                                   void* out_bf16, cudaStream_t stream)
 {
     using namespace moedc_host;
-    if (scale_layout != 0 && scale_layout != MOEDC_SCALES_COL_MAJOR) return MOEDC_ERR_ARG;
+    const int mode = scale_mode(scale_layout);
+    if (mode < 0) return MOEDC_ERR_ARG;
     if (E < 1 || E > MOEDC_MAX_E || cap < 1 || H < 128 || H % 128 != 0) return MOEDC_ERR_ARG;
     if ((int64_t)E * cap * ((H + 511) / 512) > INT32_MAX) return MOEDC_ERR_ARG;
     if (!recv || !scales || !num_tokens_per_expert || !out_bf16) return MOEDC_ERR_ARG;
@@ -119,7 +122,7 @@ extern "C" int moedc_dequant_e4m3(const void* recv, const float* scales, int sca
         resident_blocks((const void*)moedc::dequant_e4m3_kernel, moedc::kDequantThreads, 0);
     if (blocks > resident) blocks = resident;
     clear_stale_error();
-    launch(moedc::dequant_e4m3_kernel, (int)blocks, moedc::kDequantThreads, 0, stream, static_cast<const uint8_t*>(recv), scales, scale_layout != 0, num_tokens_per_expert, E,
+    launch(moedc::dequant_e4m3_kernel, (int)blocks, moedc::kDequantThreads, 0, stream, static_cast<const uint8_t*>(recv), scales, mode, num_tokens_per_expert, E,
         cap, H, static_cast<uint16_t*>(out_bf16));
     return launch_status();
 }

@@ -91,7 +91,8 @@ static bool dispatch_args_ok(const void* x, int T, int H, const int32_t* topk_id
     if (T < 0 || H < 8 || K < 1 || K > MOEDC_MAX_K || E < 1 || E > MOEDC_MAX_E || cap < 1)
         return false;
     if (!dtype_ok(out_dtype)) return false;
-    out_dtype &= ~MOEDC_SCALES_COL_MAJOR;
+    if ((out_dtype & MOEDC_SCALES_PER_TOKEN) && H > MOEDC_TOKEN_SCALE_MAX_H) return false;
+    out_dtype = dtype_base(out_dtype);
     if (out_dtype == MOEDC_BF16 && H % 8 != 0) return false;
     if (out_dtype == MOEDC_FP8_E4M3 && H % 128 != 0) return false;
     if ((int64_t)E * cap > INT32_MAX) return false;
@@ -111,6 +112,9 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
                     void* recv, float* scales, int32_t* src_idx, int32_t* dev_status,
                     cudaStream_t stream)
 {
+    if (out_dtype & MOEDC_SCALES_PER_TOKEN)
+        return launch_dispatch_token(x, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap,
+                                     recv, scales, src_idx, dev_status, stream);
     const int warps_per_block = moedc::kDispatchThreads / moedc::kWarp;
     const int nslice = (H + moedc::kSlice - 1) / moedc::kSlice;
     const int64_t items = (int64_t)T * nslice;

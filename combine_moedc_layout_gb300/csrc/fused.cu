@@ -253,7 +253,9 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     if (!layout_args_ok(T, K, E, R, cap)) return MOEDC_ERR_ARG;
     if (!dtype_ok(out_dtype)) return MOEDC_ERR_ARG;
     const bool cols = (out_dtype & MOEDC_SCALES_COL_MAJOR) != 0;
-    const int base = out_dtype & ~MOEDC_SCALES_COL_MAJOR;
+    const bool per_token = (out_dtype & MOEDC_SCALES_PER_TOKEN) != 0;
+    const int base = dtype_base(out_dtype);
+    if (per_token && H > MOEDC_TOKEN_SCALE_MAX_H) return MOEDC_ERR_ARG;
     if (H < 8 || (base == MOEDC_BF16 && H % 8 != 0) || (base == MOEDC_FP8_E4M3 && H % 128 != 0))
         return MOEDC_ERR_ARG;
     if (base == MOEDC_FP8_E4M3 && (int64_t)E * cap * (H / 128) > INT32_MAX) return MOEDC_ERR_ARG;
@@ -269,7 +271,7 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
         return MOEDC_ERR_ARG;
 
     const int64_t n = (int64_t)T * K;
-    if (n > MOEDC_FUSED_MAX_ENTRIES) {
+    if (n > MOEDC_FUSED_MAX_ENTRIES || per_token) {   // a row's scale needs all its slices
         const LayoutGeom g = layout_geometry(T, K, E, R);
         if (g.ws > 0 && (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)))
             return MOEDC_ERR_ARG;

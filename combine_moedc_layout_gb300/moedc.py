@@ -30,6 +30,8 @@ ERR_UNIMPLEMENTED = 6
 BF16 = 0
 FP8_E4M3 = 1
 SCALES_COL_MAJOR = 0x100    # OR into FP8_E4M3: scales stored [E, H/128, cap]
+SCALES_PER_TOKEN = 0x200    # OR into FP8_E4M3: one scale per row, scales [E, cap]
+TOKEN_SCALE_MAX_H = 32768   # MOEDC_TOKEN_SCALE_MAX_H
 
 EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes",
             "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
@@ -239,10 +241,12 @@ def layout(topk_idx: torch.Tensor, E: int, R: int, cap: int,
 
 def alloc_recv(E: int, cap: int, H: int, out_dtype: int, device):
     """recv [E,cap,H] (bf16, or e4m3 as torch.float8_e4m3fn), scales [E,cap,H/128]
-    ([E,H/128,cap] with SCALES_COL_MAJOR; fp32, e4m3 only) and src_idx [E,cap]."""
-    if out_dtype & ~SCALES_COL_MAJOR == FP8_E4M3:
+    ([E,H/128,cap] with SCALES_COL_MAJOR, [E,cap] with SCALES_PER_TOKEN; fp32,
+    e4m3 only) and src_idx [E,cap]."""
+    if out_dtype & ~(SCALES_COL_MAJOR | SCALES_PER_TOKEN) == FP8_E4M3:
         recv = torch.empty((E, cap, H), dtype=torch.float8_e4m3fn, device=device)
-        shape = (E, H // 128, cap) if out_dtype & SCALES_COL_MAJOR else (E, cap, H // 128)
+        shape = ((E, cap) if out_dtype & SCALES_PER_TOKEN
+                 else (E, H // 128, cap) if out_dtype & SCALES_COL_MAJOR else (E, cap, H // 128))
         scales = torch.empty(shape, dtype=torch.float32, device=device)
     else:
         recv = torch.empty((E, cap, H), dtype=torch.bfloat16, device=device)
@@ -315,7 +319,8 @@ def dequant_e4m3(recv: torch.Tensor, scales: torch.Tensor, num_tokens_per_expert
 def combine_e4m3(expert_out: torch.Tensor, expert_scales: torch.Tensor, topk_idx: torch.Tensor,
                  slot: torch.Tensor, topk_weights: torch.Tensor, scale_layout: int = 0,
                  status: torch.Tensor | None = None) -> torch.Tensor:
-    """Combine from e4m3 expert outputs [E, cap, H] with per-128 fp32 scales."""
+    """Combine from e4m3 expert outputs [E, cap, H] with fp32 scales in the
+    given scale_layout (0, SCALES_COL_MAJOR or SCALES_PER_TOKEN)."""
     _need(topk_weights, torch.float32, "topk_weights")
     E, cap, H = expert_out.shape
     T, K = topk_idx.shape

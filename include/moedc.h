@@ -98,6 +98,14 @@ typedef enum { MOEDC_BF16 = 0, MOEDC_FP8_E4M3 = 1 } moedc_dtype;
  * GEMM reads per K-block) instead of [E][cap][G].  Codes are unchanged. */
 #define MOEDC_SCALES_COL_MAJOR 0x100
 
+/* OR-ed into the out_dtype of moedc_dispatch / moedc_layout_dispatch with
+ * MOEDC_FP8_E4M3 instead of MOEDC_SCALES_COL_MAJOR: one scale per token row
+ * (the 128-channel rule with the group widened to all H channels), scales
+ * [E][cap].  Also a scale_layout of moedc_dequant_e4m3 / moedc_combine_e4m3.
+ * H <= MOEDC_TOKEN_SCALE_MAX_H with this flag. */
+#define MOEDC_SCALES_PER_TOKEN 0x200
+#define MOEDC_TOKEN_SCALE_MAX_H 32768
+
 /* Limits checked on the host (MOEDC_ERR_ARG beyond them). */
 #define MOEDC_MAX_K 32
 #define MOEDC_MAX_E 1024
@@ -172,6 +180,9 @@ MOEDC_EXPORT int moedc_layout_static_scratch(const int32_t* topk_idx, int T, int
  *                   recv[e][s][128g+i] = e4m3fn(x / sc) with one binary32
  *                   division and round-to-nearest-even, saturating to +-448;
  *                   scales[e][s][g] = sc.
+ *   MOEDC_FP8_E4M3 | MOEDC_SCALES_PER_TOKEN: the same with a single group of
+ *                   all H channels: a = max over the row, scales[e][s] = sc
+ *                   ([E][cap]); H <= MOEDC_TOKEN_SCALE_MAX_H.
  * src_idx[e][s] = -1 for every s in [num_tokens_per_expert[e], cap).
  * Rows of recv / scales that no entry reaches are not written.
  * num_tokens_per_expert and slot are the outputs of moedc_layout for the same
@@ -209,7 +220,8 @@ MOEDC_EXPORT int moedc_combine(const void* expert_out, int E, int cap, int H,
  * and channel h of group g = h / 128:
  *   out[e][s][h] = bf16_rne( float(recv[e][s][h]) * scales[e][s][g] )
  * with one binary32 multiply.  Rows past an expert's count are not written.
- * scale_layout: 0 for scales [E][cap][G], MOEDC_SCALES_COL_MAJOR for [E][G][cap].
+ * scale_layout: 0 for scales [E][cap][G], MOEDC_SCALES_COL_MAJOR for [E][G][cap],
+ * MOEDC_SCALES_PER_TOKEN for one scale per row [E][cap] (every g uses it).
  * recv and out must be 16-byte aligned; H % 128 == 0.  No data errors.
  */
 MOEDC_EXPORT int moedc_dequant_e4m3(const void* recv, const float* scales, int scale_layout,
@@ -217,8 +229,9 @@ MOEDC_EXPORT int moedc_dequant_e4m3(const void* recv, const float* scales, int s
                  void* out_bf16, cudaStream_t stream);
 
 /*
- * Combine from e4m3 expert outputs with per-128-channel fp32 scales (the
- * same format dispatch produces; scale_layout as for moedc_dequant_e4m3):
+ * Combine from e4m3 expert outputs with fp32 scales (the formats dispatch
+ * produces; scale_layout as for moedc_dequant_e4m3, scale(e, s, g) being
+ * scales[e][s] for every g with MOEDC_SCALES_PER_TOKEN):
  *   y[t][h] = bf16_rne( sum over k ascending of
  *                       w[t][k] * (float(expert_out[e][s][h]) * scale(e, s, h/128)) )
  * binary32 accumulator from +0, each product rounded, never fused; masked,
@@ -246,7 +259,8 @@ MOEDC_EXPORT int moedc_combine_e4m3(const void* expert_out, const float* expert_
  * moedc_rank_dispatch: for each (t, r) with j = rank_slot[t][r] in [0, cap_rank):
  *   rank_src_idx[r][j] = t; recv_rank[r][j][:] = x[t][:] (MOEDC_BF16), or the
  *   e4m3 codes and per-128 fp32 scales of x[t] by the moedc_dispatch rule
- *   (MOEDC_FP8_E4M3, scales_rank [R, cap_rank, H/128]).  rank_src_idx = -1
+ *   (MOEDC_FP8_E4M3, scales_rank [R, cap_rank, H/128]; the scale-layout
+ *   flags are not offered here: MOEDC_ERR_ARG).  rank_src_idx = -1
  *   for j in [num_tokens_per_rank[r], cap_rank); other rows are not written.
  *
  * moedc_rank_combine: each rank returns one bf16 partial row per received
@@ -275,7 +289,8 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * synchronisation), the blocks split the (token, 512-channel slice) copies,
  * and each layout output is written by the warp that owns it (a token's slots
  * and rank flags by the warp copying its first slice, a rank's count by one
- * warp, the expert counts by block 0).  Larger inputs run moedc_layout and
+ * warp, the expert counts by block 0).  MOEDC_SCALES_PER_TOKEN always takes the
+ * two-launch path (a row's scale needs all of its slices).  Larger inputs run moedc_layout and
  * moedc_dispatch back to back.  Results are identical either way.
  * workspace: as for moedc_layout (never used on the single-launch path).
  */

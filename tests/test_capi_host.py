@@ -98,6 +98,25 @@ def test_argument_errors_return_before_cuda(lib):
     assert lib.moedc_combine_e4m3(fake, fake, 0, 8, 4, 200, fake, fake, fake, 4, 2, fake, fake,
                                   None) == moedc.ERR_ARG
     assert lib.moedc_dequant_e4m3(fake, fake, 3, fake, 8, 4, 256, fake, None) == moedc.ERR_ARG
+    # per-token scales: not with the column-major flag, not beyond the width limit, not on
+    # the rank-major path, not as a bf16 flag
+    both = moedc.FP8_E4M3 | moedc.SCALES_PER_TOKEN | moedc.SCALES_COL_MAJOR
+    assert lib.moedc_dispatch(fake, 4, 256, fake, fake, fake, 2, 8, 4, both, fake, fake, fake,
+                              fake, None) == moedc.ERR_ARG
+    tok = moedc.FP8_E4M3 | moedc.SCALES_PER_TOKEN
+    wide = moedc.TOKEN_SCALE_MAX_H + 128
+    assert lib.moedc_dispatch(fake, 4, wide, fake, fake, fake, 2, 8, 4, tok, fake, fake, fake,
+                              fake, None) == moedc.ERR_ARG
+    assert lib.moedc_layout_dispatch(fake, fake, 4, wide, 2, 8, 2, 4, tok, fake, fake, fake,
+                                     fake, fake, fake, fake, None, 0, fake, None) == moedc.ERR_ARG
+    assert lib.moedc_dispatch(fake, 4, 256, fake, fake, fake, 2, 8, 4,
+                              moedc.BF16 | moedc.SCALES_PER_TOKEN, fake, fake, fake, fake,
+                              None) == moedc.ERR_ARG
+    assert lib.moedc_rank_dispatch(fake, 4, 256, fake, fake, 2, 4, tok, fake, fake, fake,
+                                   None) == moedc.ERR_ARG
+    assert lib.moedc_combine_e4m3(fake, fake, moedc.SCALES_PER_TOKEN | moedc.SCALES_COL_MAJOR, 8,
+                                  4, 256, fake, fake, fake, 4, 2, fake, fake, None) == \
+        moedc.ERR_ARG
     assert lib.moedc_dispatch(fake, 4, 256, fake, fake, fake, 2, 8, 4,
                               moedc.BF16 | moedc.SCALES_COL_MAJOR, fake, fake, fake, fake,
                               None) == moedc.ERR_ARG
