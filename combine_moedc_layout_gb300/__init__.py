@@ -9,6 +9,7 @@ from .moedc import (BF16, FP8_E4M3, SCALES_COL_MAJOR, SCALES_PER_TOKEN, Layout, 
                     dispatch, layout, layout_dispatch, layout_workspace, load, moedc_combine,
                     moedc_dequant_e4m3, moedc_dispatch, moedc_layout, moedc_layout_dispatch,
                     moedc_layout_static_scratch, moedc_layout_workspace_bytes,
+                    moedc_layout_dispatch_workspace_bytes, layout_dispatch_workspace,
                     moedc_rank_combine, moedc_rank_dispatch, moedc_rank_layout, rank_combine,
                     rank_dispatch, rank_layout, strerror)
 
@@ -16,6 +17,7 @@ __all__ = ["BF16", "FP8_E4M3", "SCALES_COL_MAJOR", "SCALES_PER_TOKEN", "Layout",
            "combine", "combine_e4m3", "dequant_e4m3", "moedc_combine_e4m3",
            "dispatch", "layout", "layout_dispatch", "layout_workspace", "load", "moedc_combine",
            "moedc_dequant_e4m3", "moedc_dispatch", "moedc_layout", "moedc_layout_dispatch",
-           "moedc_layout_static_scratch", "moedc_layout_workspace_bytes", "moedc_rank_combine",
+           "moedc_layout_static_scratch", "moedc_layout_workspace_bytes",
+           "moedc_layout_dispatch_workspace_bytes", "layout_dispatch_workspace", "moedc_rank_combine",
            "moedc_rank_dispatch", "moedc_rank_layout", "rank_combine", "rank_dispatch",
            "rank_layout", "strerror"]

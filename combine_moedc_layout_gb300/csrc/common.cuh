@@ -24,6 +24,27 @@ __device__ __forceinline__ unsigned lanemask_lt()
     return m;
 }
 
+// Lanes of the warp holding the same expert as this lane (invalid lanes match
+// each other): the intersection, over the bits of the key e + 1 (0 when
+// invalid, at most MOEDC_MAX_E), of the lanes that agree on that bit.  Eleven
+// independent ballots; in the shared-memory layout passes of the single-launch
+// kernels the hardware match.any measured several times slower for 32 mostly
+// distinct keys.
+constexpr int kExpertKeyBits = 11;
+static_assert(MOEDC_MAX_E < (1 << kExpertKeyBits), "expert match key width");
+__device__ __forceinline__ unsigned match_expert(int e, bool valid)
+{
+    const int key = valid ? e + 1 : 0;
+    unsigned peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < kExpertKeyBits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const unsigned m = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
 // bf16 bit pattern -> binary32 (exact widening).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -177,6 +198,15 @@ int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const 
                     const int32_t* num_tokens_per_expert, int K, int E, int cap, int out_dtype,
                     void* recv, float* scales, int32_t* src_idx, int32_t* dev_status,
                     cudaStream_t stream);
+// cooperative single-launch layout + dispatch (layout_dispatch_coop.cu);
+// MOEDC_ERR_UNIMPLEMENTED when it does not apply
+size_t layout_dispatch_coop_workspace_bytes(int T, int K, int E, int R);
+int launch_layout_dispatch_coop(const void* x, const int32_t* topk_idx, int T, int H, int K,
+                                int E, int R, int cap, int out_dtype,
+                                int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                                uint8_t* is_token_in_rank, int32_t* slot, void* recv,
+                                float* scales, int32_t* src_idx, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 // e4m3 dispatch with one scale per token row (dispatch_token.cu)
 int launch_dispatch_token(const void* x, int T, int H, const int32_t* topk_idx,
                           const int32_t* slot, const int32_t* num_tokens_per_expert, int K,

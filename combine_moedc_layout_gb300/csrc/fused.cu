@@ -34,22 +34,6 @@ constexpr int kFusedIdsPerThread = 2;
 constexpr int kFusedNarrow = 128;
 constexpr int kFusedWide = MOEDC_FUSED_MAX_ENTRIES / kFusedIdsPerThread;
 static_assert(kFusedWide == 512, "wide fused block");
-constexpr int kKeyBits = 11;   // keys are expert + 1 <= MOEDC_MAX_E
-static_assert(MOEDC_MAX_E < (1 << kKeyBits), "ballot match key width");
-
-// Lanes of the warp holding the same key (0 <= key < 2^kKeyBits): the
-// intersection, over the key's bits, of the lanes that agree on that bit.
-__device__ __forceinline__ unsigned match_key(int key)
-{
-    unsigned peers = 0xffffffffu;
-#pragma unroll
-    for (int b = 0; b < kKeyBits; ++b) {
-        const bool bit = (key >> b) & 1;
-        const unsigned m = __ballot_sync(0xffffffffu, bit);
-        peers &= bit ? m : ~m;
-    }
-    return peers;
-}
 
 // Shared memory (int32 words) of one block of `threads` for n entries, E experts.
 __host__ __device__ constexpr size_t fused_smem_words(int threads, int n, int E)
@@ -133,7 +117,7 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
         const int i = i0 + lane;
         const int e = i < wend ? s_idx[i] : -1;
         const bool v = e >= 0 && e < E;
-        const unsigned peers = match_key(v ? e + 1 : 0);
+        const unsigned peers = match_expert(e, v);
         int sv = -1;
         if (v) sv = my[e] + __popc(peers & lt);
         __syncwarp();
@@ -271,6 +255,13 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
         return MOEDC_ERR_ARG;
 
     const int64_t n = (int64_t)T * K;
+    if (n > MOEDC_FUSED_MAX_ENTRIES && !per_token) {
+        const int st = launch_layout_dispatch_coop(
+            x, topk_idx, T, H, K, E, R, cap, out_dtype, num_tokens_per_expert,
+            num_tokens_per_rank, is_token_in_rank, slot, recv, scales, src_idx, workspace,
+            workspace_bytes, dev_status, stream);
+        if (st != MOEDC_ERR_UNIMPLEMENTED) return st;
+    }
     if (n > MOEDC_FUSED_MAX_ENTRIES || per_token) {   // a row's scale needs all its slices
         const LayoutGeom g = layout_geometry(T, K, E, R);
         if (g.ws > 0 && (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)))

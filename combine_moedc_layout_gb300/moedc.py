@@ -36,7 +36,8 @@ TOKEN_SCALE_MAX_H = 32768   # MOEDC_TOKEN_SCALE_MAX_H
 EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes",
             "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
             "moedc_layout_static_scratch", "moedc_dequant_e4m3", "moedc_rank_layout",
-            "moedc_rank_dispatch", "moedc_rank_combine", "moedc_combine_e4m3")
+            "moedc_rank_dispatch", "moedc_rank_combine", "moedc_combine_e4m3",
+            "moedc_layout_dispatch_workspace_bytes")
 
 STATIC_SCRATCH_BYTES = 1 << 20   # MOEDC_STATIC_SCRATCH_BYTES
 
@@ -70,6 +71,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_strerror.restype = ctypes.c_char_p
     lib.moedc_layout_workspace_bytes.argtypes = [I, I, I, I]
     lib.moedc_layout_workspace_bytes.restype = Z
+    lib.moedc_layout_dispatch_workspace_bytes.argtypes = [I, I, I, I]
+    lib.moedc_layout_dispatch_workspace_bytes.restype = Z
     lib.moedc_layout.argtypes = [P, I, I, I, I, I, P, P, P, P, P, Z, P, P]
     lib.moedc_layout.restype = I
     lib.moedc_dispatch.argtypes = [P, I, I, P, P, P, I, I, I, I, P, P, P, P, P]
@@ -122,6 +125,10 @@ def _check(code: int, where: str) -> None:
 
 def moedc_layout_workspace_bytes(T: int, K: int, E: int, R: int) -> int:
     return int(load().moedc_layout_workspace_bytes(T, K, E, R))
+
+
+def moedc_layout_dispatch_workspace_bytes(T: int, K: int, E: int, R: int) -> int:
+    return int(load().moedc_layout_dispatch_workspace_bytes(T, K, E, R))
 
 
 def moedc_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,
@@ -222,6 +229,13 @@ def layout_workspace(T: int, K: int, E: int, R: int, device) -> torch.Tensor | N
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
 
 
+def layout_dispatch_workspace(T: int, K: int, E: int, R: int, device) -> torch.Tensor | None:
+    """Workspace that lets moedc_layout_dispatch run as one launch at any T
+    (uninitialised memory is fine; do not share it between concurrent calls)."""
+    n = moedc_layout_dispatch_workspace_bytes(T, K, E, R)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
+
+
 def layout(topk_idx: torch.Tensor, E: int, R: int, cap: int,
            workspace: torch.Tensor | None = None, status: torch.Tensor | None = None) -> Layout:
     _need(topk_idx, torch.int32, "topk_idx")
@@ -296,7 +310,7 @@ def layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int, cap
                  torch.zeros(1, dtype=torch.int32, device=dev))
     recv, scales, src_idx = alloc_recv(E, cap, H, out_dtype, dev)
     if workspace is None:
-        workspace = layout_workspace(T, K, E, R, dev)
+        workspace = layout_dispatch_workspace(T, K, E, R, dev)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(moedc_layout_dispatch(x, topk_idx, T, H, K, E, R, cap, out_dtype,
                                  lay.num_tokens_per_expert, lay.num_tokens_per_rank,

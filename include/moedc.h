@@ -42,9 +42,12 @@
  *    MOEDC_ERR_CAPACITY      an expert received more than cap entries; the
  *                            slots still count on, and the entries whose slot
  *                            is >= cap are dropped by dispatch and combine.
- *  MOEDC_ERR_TIMEOUT is reserved: no kernel of this library waits on data
- *  written by another block (the only wait is the hardware's
- *  griddepcontrol.wait for the previous kernel of the stream).
+ *    MOEDC_ERR_TIMEOUT       only from the cooperative single launch of
+ *                            moedc_layout_dispatch: one of its two grid
+ *                            barriers waited out its bound (>= 0.13 s, e.g.
+ *                            when other work holds the SMs); its outputs are
+ *                            then incomplete.  No other kernel waits on data
+ *                            written by another block.
  *
  * Sources (page title, part of the page):
  *  [UCCL749]  UCCL PR #749 "[EP] Low-latency mode batch tokens per
@@ -289,12 +292,24 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * synchronisation), the blocks split the (token, 512-channel slice) copies,
  * and each layout output is written by the warp that owns it (a token's slots
  * and rank flags by the warp copying its first slice, a rank's count by one
- * warp, the expert counts by block 0).  MOEDC_SCALES_PER_TOKEN always takes the
- * two-launch path (a row's scale needs all of its slices).  Larger inputs run moedc_layout and
- * moedc_dispatch back to back.  Results are identical either way.
- * workspace: as for moedc_layout (never used on the single-launch path).
+ * warp, the expert counts by block 0).
+ * Inputs beyond the single-launch layout (T * K > 65536, where
+ * moedc_layout_workspace_bytes is nonzero) with a workspace of at least
+ * moedc_layout_dispatch_workspace_bytes(T, K, E, R) bytes are also ONE launch,
+ * a cooperative one [UCCL749 per-expert counts a rank waits on]: each block
+ * ranks and counts a contiguous chunk of tokens, a grid barrier, one block
+ * per expert / rank scans the chunks' counts, a second barrier, then each
+ * block assigns its chunk's slots and copies its chunk.  The barriers are
+ * bounded waits (MOEDC_ERR_TIMEOUT when one runs out); the workspace needs
+ * no initialisation but must not be shared by calls that can run at the same
+ * time.  In between (1024 < T * K <= 65536), with a smaller workspace (at
+ * least moedc_layout_workspace_bytes), or when a chunk would exceed 2048
+ * entries, layout and dispatch run as two launches (in between that is the
+ * faster form).  MOEDC_SCALES_PER_TOKEN always takes the two-launch path (a
+ * row's scale needs all of its slices).  Results are identical on every path.
  */
 #define MOEDC_FUSED_MAX_ENTRIES 1024
+MOEDC_EXPORT size_t moedc_layout_dispatch_workspace_bytes(int T, int K, int E, int R);
 MOEDC_EXPORT int moedc_layout_dispatch(const void* x, const int32_t* topk_idx,
                           int T, int H, int K, int E, int R, int cap, int out_dtype,
                           int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,

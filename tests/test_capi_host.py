@@ -64,6 +64,15 @@ def test_workspace_bytes(lib):
     # beyond: 128 tokens per block -> blocks x (E + R) int32
     assert moedc.moedc_layout_workspace_bytes(8193, 8, 256, 8) == 65 * (256 + 8) * 4
     assert moedc.moedc_layout_workspace_bytes(40000, 8, 128, 8) == 313 * (128 + 8) * 4
+    # the one-call layout+dispatch: none while the layout is one sweep launch
+    # (fused block, or layout then dispatch), beyond it the cooperative
+    # launch's barrier words and count rows [E + R][2048]
+    assert moedc.moedc_layout_dispatch_workspace_bytes(128, 8, 288, 8) == 0
+    assert moedc.moedc_layout_dispatch_workspace_bytes(4096, 8, 256, 8) == 0
+    assert moedc.moedc_layout_dispatch_workspace_bytes(8192, 8, 256, 8) == 0
+    assert moedc.moedc_layout_dispatch_workspace_bytes(8193, 8, 256, 8) == 256 + 264 * 2048 * 4
+    assert moedc.moedc_layout_dispatch_workspace_bytes(40000, 8, 128, 8) == 256 + 136 * 2048 * 4
+    assert moedc.moedc_layout_dispatch_workspace_bytes(4096, 8, 250, 8) == 0
     # rejected shapes report 0
     assert moedc.moedc_layout_workspace_bytes(4096, 8, 250, 8) == 0
     assert moedc.moedc_layout_workspace_bytes(4096, 0, 256, 8) == 0
