@@ -265,7 +265,10 @@ def side_workloads(dev) -> dict:
     they are latencies, not HBM rates.  imbalanced: layout, bf16 dispatch and
     combine back to back, us and algorithmic GB/s per kernel.  rank_major: the
     same 4096-token e4m3 workload through rank layout, rank dispatch and rank
-    combine (one row per token and destination rank).
+    combine (one row per token and destination rank).  combine_e4m3: combine
+    from e4m3 rows.  dispatch_token_scale: e4m3 dispatch with one scale per
+    token row.  large_t_layout_dispatch: moedc_layout_dispatch at 40000 tokens
+    as one cooperative launch and as layout then dispatch.
     """
     import torch
 
@@ -477,6 +480,69 @@ def side_workloads(dev) -> dict:
     out["combine_e4m3"] = {"T": T, "H": H, "K": K, "E": E, "algorithmic_bytes": cb, "us_mean": m,
                            "us_median": us[len(us) // 2], "gbs": cb / (m * 1e-6) / 1e9,
                            "note": "back-to-back launches: the e4m3 rows (235 MB) partly stay in L2"}
+    del recv, scales
+
+    flush = torch.empty(256 << 20, dtype=torch.float32, device=dev)
+
+    def flushed_us(fn):
+        """median device us of fn, each call after a 1 GiB write that evicts L2"""
+        for _ in range(5):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        v = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        return v[len(v) // 2]
+
+    # e4m3 dispatch with one scale per token row, same layout as above
+    tok = moedc.FP8_E4M3 | moedc.SCALES_PER_TOKEN
+    recv, scales, src = moedc.alloc_recv(E, cap, H, tok, dev)
+
+    def tok_call():
+        if moedc.moedc_dispatch(x, T, H, idx, sl, cnt, K, E, cap, tok, recv, scales, src, st,
+                                stream) != 0:
+            raise RuntimeError("moedc_dispatch (per-token scales) failed")
+
+    tb = 2 * H * T + N * (H + 4) + 8 * T * K + 4 * E * cap
+    us_tok = flushed_us(tok_call)
+    out["dispatch_token_scale"] = {"T": T, "H": H, "K": K, "E": E, "algorithmic_bytes": tb,
+                                   "us_median": us_tok, "gbs": tb / (us_tok * 1e-6) / 1e9,
+                                   "timing": "L2 evicted before each call"}
+    del recv, scales, src
+
+    # one-call layout+dispatch beyond the single-launch layout (320000 entries):
+    # the cooperative single launch against layout then dispatch
+    c = synth.make_random_case(91, T=40000, H=128, K=8, E=128, R=8, cap=None, dtype=synth.BF16,
+                               mask_p=0.01)
+    T, H, K, E, R, cap = c.T, c.H, c.K, c.E, c.R, c.cap
+    x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(c.topk_idx).to(dev)
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    rk = torch.empty(R, dtype=torch.int32, device=dev)
+    inr = torch.empty((T, R), dtype=torch.uint8, device=dev)
+    sl = torch.empty((T, K), dtype=torch.int32, device=dev)
+    recv, scales, src = moedc.alloc_recv(E, cap, H, c.dtype, dev)
+    res = {"T": T, "H": H, "K": K, "E": E, "R": R, "cap": cap, "dtype": "bf16",
+           "timing": "L2 evicted before each call"}
+    for name, nbytes in (("single_cooperative_launch_us",
+                          moedc.moedc_layout_dispatch_workspace_bytes(T, K, E, R)),
+                         ("layout_then_dispatch_us", moedc.moedc_layout_workspace_bytes(T, K, E, R))):
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+
+        def ld_call():
+            if moedc.moedc_layout_dispatch(x, idx, T, H, K, E, R, cap, c.dtype, cnt, rk, inr, sl,
+                                           recv, scales, src, ws, nbytes, st, stream) != 0:
+                raise RuntimeError("moedc_layout_dispatch failed")
+
+        res[name] = flushed_us(ld_call)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"large-T layout+dispatch: device status {int(st.item())}")
+    out["large_t_layout_dispatch"] = res
     return out
 
 
