@@ -307,6 +307,10 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * entries, layout and dispatch run as two launches (in between that is the
  * faster form).  MOEDC_SCALES_PER_TOKEN always takes the two-launch path (a
  * row's scale needs all of its slices).  Results are identical on every path.
+ * Test hook: with the environment variable MOEDC_TEST_BARRIER_EXTRA=n set,
+ * the cooperative launch's barriers wait for n blocks more than the grid has,
+ * so that they run out and report MOEDC_ERR_TIMEOUT; it exists to test that
+ * path and is never set in normal use.
  */
 #define MOEDC_FUSED_MAX_ENTRIES 1024
 MOEDC_EXPORT size_t moedc_layout_dispatch_workspace_bytes(int T, int K, int E, int R);
