@@ -48,6 +48,10 @@ RANDOM = {
                         scale=1e30),
     "large_t": dict(seed=22, T=40000, H=128, K=8, E=128, R=8, cap=None, dtype=synth.BF16,
                     mask_p=0.01),
+    # the widest rows: 128 slices of 512 channels (bf16), 64 (e4m3)
+    "h65536_bf16": dict(seed=28, T=40, H=65536, K=4, E=8, R=2, cap=None, dtype=synth.BF16,
+                        mask_p=0.05),
+    "h32768_fp8": dict(seed=29, T=33, H=32768, K=3, E=6, R=3, cap=None, dtype=synth.FP8_E4M3),
     # single-launch layout+dispatch: both block widths, the width boundary
     # (256 entries narrow, 257 wide), the largest shared-memory block (1024
     # entries, 1024 experts) and more ranks than the grid has warps
