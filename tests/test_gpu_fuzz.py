@@ -105,3 +105,75 @@ def test_graph_replay_rank_path_and_e4m3_combine():
 
     _graph_vs_eager(fn, [rslot, rsrc, yr, src, y])
     assert int(lay.status.item()) == 0
+
+
+def _token_shape(seed):
+    rng = np.random.default_rng(2000 + seed)
+    R = int(rng.choice([1, 2, 4, 8]))
+    E = R * int(rng.integers(1, 33))
+    K = int(rng.integers(1, min(E, 10) + 1))
+    T = int(rng.choice([1, 3, 40, 257, 2000]))
+    H = 128 * int(rng.choice([1, 3, 5, 14, 56, 130, 256]))
+    return dict(seed=seed, T=T, H=H, K=K, E=E, R=R, cap=None, dtype=synth.FP8_E4M3,
+                mask_p=float(rng.choice([0.0, 0.1])), distinct=bool(rng.integers(0, 2)) and K <= E)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_token_scale(seed):
+    """Per-token e4m3 scales through dispatch, dequant and e4m3 combine."""
+    c = synth.make_random_case(**_token_shape(seed))
+    d = DevCase(c)
+    tok = moedc.FP8_E4M3 | moedc.SCALES_PER_TOKEN
+    lay = run_layout(d)
+    recv, scales, src = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, tok)
+    deq = moedc.dequant_e4m3(recv, scales, lay.num_tokens_per_expert,
+                             scale_layout=moedc.SCALES_PER_TOKEN)
+    y = moedc.combine_e4m3(recv, scales, d.topk_idx, lay.slot, d.topk_weights,
+                           scale_layout=moedc.SCALES_PER_TOKEN)
+    torch.cuda.synchronize()
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    ref = oracle.dispatch_token_scale(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap)
+    np.testing.assert_array_equal(src.cpu().numpy(), ref["src_idx"])
+    rows = valid_rows(ref_lay["num_tokens_per_expert"], c.cap)
+    if rows.size:
+        ridx = torch.from_numpy(rows).cuda()
+        np.testing.assert_array_equal(bits_host(recv.reshape(c.E * c.cap, c.H).index_select(0, ridx)),
+                                      ref["recv"].reshape(c.E * c.cap, c.H)[rows])
+        np.testing.assert_array_equal(scales.reshape(-1).index_select(0, ridx).cpu().numpy().view(np.uint32),
+                                      ref["scales"].reshape(-1)[rows].view(np.uint32))
+        ref_deq = oracle.dequant_e4m3_token(ref["recv"], ref["scales"], ref_lay["num_tokens_per_expert"])
+        np.testing.assert_array_equal(bits_host(deq.reshape(c.E * c.cap, c.H).index_select(0, ridx)),
+                                      ref_deq.reshape(c.E * c.cap, c.H)[rows])
+    ref_y = oracle.combine_e4m3(ref["recv"], ref["scales"], c.topk_idx, ref_lay["slot"],
+                                c.topk_weights, per_token=True)["y"]
+    compare_combine(y, ref_y)
+
+
+def _coop_shape(seed):
+    rng = np.random.default_rng(3000 + seed)
+    K = int(rng.choice([1, 4, 8, 16]))
+    T = int(rng.integers(65536 // K + 1, 65536 // K + 30000))
+    R = int(rng.choice([1, 2, 8, 16]))
+    E = R * int(rng.integers(1, 17))
+    K = min(K, E)
+    T = max(T, 65536 // K + 1)
+    fp8 = bool(rng.integers(0, 2))
+    return dict(seed=seed, T=T, H=128 * int(rng.integers(1, 3)) if fp8 else 8 * int(rng.integers(2, 40)),
+                K=K, E=E, R=R, cap=None, dtype=synth.FP8_E4M3 if fp8 else synth.BF16,
+                mask_p=float(rng.choice([0.0, 0.03])), distinct=bool(rng.integers(0, 2)))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fuzz_cooperative_layout_dispatch(seed):
+    """Random shapes beyond 65536 routing entries through the one-call
+    layout+dispatch, which runs as one cooperative launch there."""
+    c = synth.make_random_case(**_coop_shape(seed))
+    assert c.T * c.K > 65536
+    d = DevCase(c)
+    lay, recv, scales, src = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, c.dtype)
+    torch.cuda.synchronize()
+    ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    compare_layout(lay, ref_lay, c.T)
+    ref_d = oracle.dispatch(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap,
+                            fp8=c.dtype == synth.FP8_E4M3)
+    compare_dispatch(c, recv, scales, src, ref_lay, ref_d)
