@@ -41,38 +41,20 @@ __host__ __device__ constexpr size_t fused_smem_words(int threads, int n, int E)
     return 2 * (size_t)n + (size_t)(threads / kWarp + 1) * E;
 }
 
-template <int kThreads, bool kFp8, bool kScaleCols>
-__global__ void __launch_bounds__(kThreads)
-fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
-                             int T, int H, int K, int E, int R, int cap,
-                             int32_t* __restrict__ num_tokens_per_expert,
-                             int32_t* __restrict__ num_tokens_per_rank,
-                             uint8_t* __restrict__ is_token_in_rank, int32_t* __restrict__ slot,
-                             void* __restrict__ recv, float* __restrict__ scales,
-                             int32_t* __restrict__ src_idx, int32_t* __restrict__ status)
+// The layout of all n entries, rebuilt in this block's shared memory: each
+// warp owns a contiguous run of 32-entry tiles in (t, k) order; the run is
+// counted per expert, the counts are scanned across warps, then equal
+// experts are ranked inside each tile in lane order.  On return s_idx holds
+// the routing ids, s_slot the slots (-1 for masked / out-of-range entries) and
+// s_cnt the per-expert counts.
+template <int kThreads>
+__device__ __forceinline__ void block_layout(const int32_t* __restrict__ topk_idx, int n, int E,
+                                             int32_t* s_idx, int32_t* s_slot, int32_t* s_wcnt,
+                                             int32_t* s_cnt)
 {
     constexpr int kFusedWarps = kThreads / kWarp;
-    pdl_enter();
-    extern __shared__ int32_t smem[];
-    const int n = T * K;                        // <= kThreads * kFusedIdsPerThread
-    int32_t* s_idx = smem;                      // [n]
-    int32_t* s_slot = s_idx + n;                // [n]
-    int32_t* s_wcnt = s_slot + n;               // [kFusedWarps][E] per-warp counts, then offsets
-    int32_t* s_cnt = s_wcnt + kFusedWarps * E;  // [E] totals
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
-    const int epr = E / R;
-    const int nslice = (H + kSlice - 1) / kSlice;
-    const int items = T * nslice;
-    const int nwarps = gridDim.x * kFusedWarps;
-
-    // the warp's first x slice does not depend on the layout: start it now
-    int item = blockIdx.x * kFusedWarps + warp;
-    SliceX xv{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (item < items) {
-        const int t = item / nslice;
-        xv = load_slice<kFp8>(x + (int64_t)t * H, H, item - t * nslice, lane);
-    }
     {
         int v[kFusedIdsPerThread];
 #pragma unroll
@@ -88,10 +70,6 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
         }
     }
     __syncthreads();
-
-    // layout: each warp owns a contiguous run of 32-entry tiles in (t, k)
-    // order; count the run per expert, scan the counts across warps, then
-    // rank equal experts inside each tile in lane order
     const int run = ((n + kFusedWarps * kWarp - 1) / (kFusedWarps * kWarp)) * kWarp;
     const int wbeg = min(n, warp * run);
     const int wend = min(n, wbeg + run);
@@ -126,14 +104,30 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
         if (i < wend) s_slot[i] = sv;
     }
     __syncthreads();
+}
 
+// The layout outputs no single warp owns: the expert counts (block 0, with
+// the capacity check), each rank's distinct-token count (one warp of the grid
+// per rank), and src_idx = -1 past each expert's count (grid-strided).
+template <int kThreads>
+__device__ __forceinline__ void publish_counts(int T, int K, int E, int R, int cap,
+                                               const int32_t* s_idx, const int32_t* s_cnt,
+                                               int32_t* __restrict__ num_tokens_per_expert,
+                                               int32_t* __restrict__ num_tokens_per_rank,
+                                               int32_t* __restrict__ src_idx,
+                                               int32_t* __restrict__ status)
+{
+    constexpr int kFusedWarps = kThreads / kWarp;
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int epr = E / R;
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e < E; e += kThreads) {
             num_tokens_per_expert[e] = s_cnt[e];
             if (s_cnt[e] > cap) raise_status(status, MOEDC_ERR_CAPACITY);
         }
     }
-    // distinct tokens per rank: one warp of the grid per rank
+    const int nwarps = gridDim.x * kFusedWarps;
     for (int r = blockIdx.x * kFusedWarps + warp; r < R; r += nwarps) {
         const unsigned lo = (unsigned)(r * epr);
         int c = 0;
@@ -145,42 +139,86 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
         c = __reduce_add_sync(0xffffffffu, c);
         if (lane == 0) num_tokens_per_rank[r] = c;
     }
-
-    // src_idx: -1 past each expert's count (grid-strided), t for filled slots
-    {
-        const int64_t total = (int64_t)E * cap;
-        const int64_t nthreads = (int64_t)gridDim.x * kThreads;
-        for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
-             i += nthreads) {
-            const int e = (int)(i / cap);
-            const int s = (int)(i - (int64_t)e * cap);
-            if (s >= s_cnt[e]) src_idx[i] = -1;
-        }
+    const int64_t total = (int64_t)E * cap;
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += nthreads) {
+        const int e = (int)(i / cap);
+        const int s = (int)(i - (int64_t)e * cap);
+        if (s >= s_cnt[e]) src_idx[i] = -1;
     }
+}
+
+// A token's entries, published by the one warp that handles the token's
+// first slice: its slots, src_idx of its rows, the expert-range check, and
+// its token-in-rank row.
+__device__ __forceinline__ void publish_token(int t, int lane, int K, int E, int R, int cap,
+                                              const int32_t* s_idx, const int32_t* s_slot,
+                                              int32_t* __restrict__ slot,
+                                              uint8_t* __restrict__ is_token_in_rank,
+                                              int32_t* __restrict__ src_idx,
+                                              int32_t* __restrict__ status)
+{
+    const int epr = E / R;
+    if (lane < K) {
+        const int e = s_idx[t * K + lane];
+        const int sv = s_slot[t * K + lane];
+        const int row = dest_row(e, sv, E, cap);
+        slot[t * K + lane] = sv;
+        if (e < -1 || e >= E) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+        if (row >= 0) src_idx[row] = t;
+    }
+    for (int r = lane; r < R; r += kWarp) {
+        const unsigned lo = (unsigned)(r * epr);
+        uint8_t flag = 0;
+        for (int k = 0; k < K; ++k)
+            flag |= ((unsigned)s_idx[t * K + k] - lo < (unsigned)epr) ? 1 : 0;
+        is_token_in_rank[(int64_t)t * R + r] = flag;
+    }
+}
+
+template <int kThreads, bool kFp8, bool kScaleCols>
+__global__ void __launch_bounds__(kThreads)
+fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_idx,
+                             int T, int H, int K, int E, int R, int cap,
+                             int32_t* __restrict__ num_tokens_per_expert,
+                             int32_t* __restrict__ num_tokens_per_rank,
+                             uint8_t* __restrict__ is_token_in_rank, int32_t* __restrict__ slot,
+                             void* __restrict__ recv, float* __restrict__ scales,
+                             int32_t* __restrict__ src_idx, int32_t* __restrict__ status)
+{
+    constexpr int kFusedWarps = kThreads / kWarp;
+    pdl_enter();
+    extern __shared__ int32_t smem[];
+    const int n = T * K;                        // <= kThreads * kFusedIdsPerThread
+    int32_t* s_idx = smem;                      // [n]
+    int32_t* s_slot = s_idx + n;                // [n]
+    int32_t* s_wcnt = s_slot + n;               // [kFusedWarps][E] per-warp counts, then offsets
+    int32_t* s_cnt = s_wcnt + kFusedWarps * E;  // [E] totals
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int nslice = (H + kSlice - 1) / kSlice;
+    const int items = T * nslice;
+    const int nwarps = gridDim.x * kFusedWarps;
+
+    // the warp's first x slice does not depend on the layout: start it now
+    int item = blockIdx.x * kFusedWarps + warp;
+    SliceX xv{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (item < items) {
+        const int t = item / nslice;
+        xv = load_slice<kFp8>(x + (int64_t)t * H, H, item - t * nslice, lane);
+    }
+    block_layout<kThreads>(topk_idx, n, E, s_idx, s_slot, s_wcnt, s_cnt);
+    publish_counts<kThreads>(T, K, E, R, cap, s_idx, s_cnt, num_tokens_per_expert,
+                             num_tokens_per_rank, src_idx, status);
 
     for (; item < items; item += nwarps) {
         const int t = item / nslice;
         const int sl = item - t * nslice;
         int my_row = -1;
-        if (lane < K) {
-            const int e = s_idx[t * K + lane];
-            const int sv = s_slot[t * K + lane];
-            my_row = dest_row(e, sv, E, cap);
-            if (sl == 0) {   // the warp copying a token's first slice publishes its entries
-                slot[t * K + lane] = sv;
-                if (e < -1 || e >= E) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
-                if (my_row >= 0) src_idx[my_row] = t;
-            }
-        }
-        if (sl == 0) {
-            for (int r = lane; r < R; r += kWarp) {
-                const unsigned lo = (unsigned)(r * epr);
-                uint8_t flag = 0;
-                for (int k = 0; k < K; ++k)
-                    flag |= ((unsigned)s_idx[t * K + k] - lo < (unsigned)epr) ? 1 : 0;
-                is_token_in_rank[(int64_t)t * R + r] = flag;
-            }
-        }
+        if (lane < K) my_row = dest_row(s_idx[t * K + lane], s_slot[t * K + lane], E, cap);
+        if (sl == 0)
+            publish_token(t, lane, K, E, R, cap, s_idx, s_slot, slot, is_token_in_rank, src_idx,
+                          status);
         const int64_t sbase = kScaleCols ? colmajor_scale_base(my_row, cap, H / 128) : 0;
         store_slice<kFp8, kScaleCols>(xv, H, sl, lane, K, my_row, recv, scales, sbase, cap);
         const int next = item + nwarps;
@@ -191,13 +229,114 @@ fused_layout_dispatch_kernel(const uint16_t* __restrict__ x, const int32_t* __re
     }
 }
 
+// The same with one e4m3 scale per token row: a block owns one token at a
+// time (wide blocks: warp w holds slices w, w + 16, ... in registers), the
+// warps' maxima meet in shared memory behind one barrier per token (double
+// buffered), then every warp quantises its slices and stores the copies.
+template <int kJ>
+__global__ void __launch_bounds__(kFusedWide)
+fused_layout_dispatch_token_kernel(const uint16_t* __restrict__ x,
+                                   const int32_t* __restrict__ topk_idx, int T, int H, int K,
+                                   int E, int R, int cap,
+                                   int32_t* __restrict__ num_tokens_per_expert,
+                                   int32_t* __restrict__ num_tokens_per_rank,
+                                   uint8_t* __restrict__ is_token_in_rank,
+                                   int32_t* __restrict__ slot, uint8_t* __restrict__ recv,
+                                   float* __restrict__ scales, int32_t* __restrict__ src_idx,
+                                   int32_t* __restrict__ status)
+{
+    constexpr int kFusedWarps = kFusedWide / kWarp;
+    pdl_enter();
+    extern __shared__ int32_t smem[];
+    __shared__ float s_amax[2][kFusedWarps];
+    const int n = T * K;
+    int32_t* s_idx = smem;
+    int32_t* s_slot = s_idx + n;
+    int32_t* s_wcnt = s_slot + n;
+    int32_t* s_cnt = s_wcnt + kFusedWarps * E;
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int nslice = (H + kSlice - 1) / kSlice;
+
+    // the block's first token's slices do not depend on the layout: start them now
+    SliceX v[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+        const int sl = warp + j * kFusedWarps;
+        v[j] = SliceX{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if ((int)blockIdx.x < T && sl < nslice)
+            v[j] = load_slice_fp8(x + (int64_t)blockIdx.x * H, H, sl, lane);
+    }
+    block_layout<kFusedWide>(topk_idx, n, E, s_idx, s_slot, s_wcnt, s_cnt);
+    publish_counts<kFusedWide>(T, K, E, R, cap, s_idx, s_cnt, num_tokens_per_expert,
+                               num_tokens_per_rank, src_idx, status);
+
+    int buf = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, buf ^= 1) {
+        if (t != (int)blockIdx.x) {
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                const int sl = warp + j * kFusedWarps;
+                v[j] = SliceX{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+                if (sl < nslice) v[j] = load_slice_fp8(x + (int64_t)t * H, H, sl, lane);
+            }
+        }
+        int my_row = -1;
+        if (lane < K) my_row = dest_row(s_idx[t * K + lane], s_slot[t * K + lane], E, cap);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+            const uint32_t w[8] = {v[j].a.x, v[j].a.y, v[j].a.z, v[j].a.w,
+                                   v[j].b.x, v[j].b.y, v[j].b.z, v[j].b.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        }
+#pragma unroll
+        for (int d = kWarp / 2; d > 0; d >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        if (lane == 0) s_amax[buf][warp] = amax;
+        __syncthreads();   // one per token; the other buffer is written next time
+        float a = 0.0f;
+        for (int w = 0; w < kFusedWarps; ++w) a = fmaxf(a, s_amax[buf][w]);
+        a = fmaxf(a, 1e-4f);
+        const float sc = __fdiv_rn(a, 448.0f);
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+            const int sl = warp + j * kFusedWarps;
+            if (sl >= nslice) continue;   // uniform across the warp
+            const int c0 = sl * kSlice + lane * 16;
+            const uint32_t w[8] = {v[j].a.x, v[j].a.y, v[j].a.z, v[j].a.w,
+                                   v[j].b.x, v[j].b.y, v[j].b.z, v[j].b.w};
+            uint32_t p[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t lo = quant_pair(bf16_lo(w[2 * q]), bf16_hi(w[2 * q]), sc);
+                const uint32_t hi = quant_pair(bf16_lo(w[2 * q + 1]), bf16_hi(w[2 * q + 1]), sc);
+                p[q] = lo | (hi << 16);
+            }
+            const uint4 qv = make_uint4(p[0], p[1], p[2], p[3]);
+            for (int k = 0; k < K; ++k) {
+                const int row = __shfl_sync(0xffffffffu, my_row, k);
+                if (row >= 0 && c0 < H)
+                    st_global_cs(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), qv);
+            }
+        }
+        if (warp == 0) {
+            publish_token(t, lane, K, E, R, cap, s_idx, s_slot, slot, is_token_in_rank, src_idx,
+                          status);
+            if (lane < K && my_row >= 0) st_global_cs_f32(scales + my_row, sc);
+        }
+    }
+}
+
 }  // namespace moedc
 
 namespace {
 
 // The wide block at its largest (1024 entries, MOEDC_MAX_E experts) needs
 // more than the default 48 KB of dynamic shared memory: raise the limit of
-// its three instances once.  The attribute is per function and per device.
+// its instances once.  The attribute is per function and per device.
 // (The narrow block needs at most 2 * 256 + 5 * MOEDC_MAX_E words, 22.5 KB.)
 constexpr int kMaxDevices = 64;
 std::mutex g_smem_mutex;
@@ -217,6 +356,12 @@ bool fused_smem_ready()
         cudaFuncSetAttribute(moedc::fused_layout_dispatch_kernel<W, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(moedc::fused_layout_dispatch_kernel<W, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(moedc::fused_layout_dispatch_token_kernel<1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(moedc::fused_layout_dispatch_token_kernel<2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(moedc::fused_layout_dispatch_token_kernel<4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return false;
     g_smem_set[dev] = true;
@@ -262,7 +407,7 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
             workspace_bytes, dev_status, stream);
         if (st != MOEDC_ERR_UNIMPLEMENTED) return st;
     }
-    if (n > MOEDC_FUSED_MAX_ENTRIES || per_token) {   // a row's scale needs all its slices
+    if (n > MOEDC_FUSED_MAX_ENTRIES) {
         const LayoutGeom g = layout_geometry(T, K, E, R);
         if (g.ws > 0 && (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)))
             return MOEDC_ERR_ARG;
@@ -275,6 +420,35 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
     }
 
     const int nslice = (H + moedc::kSlice - 1) / moedc::kSlice;
+    if (per_token) {   // a block owns whole tokens: a row's scale needs all its slices
+        constexpr int W = moedc::kFusedWide;
+        const int per_warp = (nslice + W / moedc::kWarp - 1) / (W / moedc::kWarp);   // 1 .. 4
+        const void* fn = per_warp == 1   ? (const void*)moedc::fused_layout_dispatch_token_kernel<1>
+                         : per_warp == 2 ? (const void*)moedc::fused_layout_dispatch_token_kernel<2>
+                                         : (const void*)moedc::fused_layout_dispatch_token_kernel<4>;
+        if (!fused_smem_ready()) return MOEDC_ERR_CUDA;
+        const size_t sm = moedc::fused_smem_words(W, (int)n, E) * sizeof(int32_t);
+        const int64_t fill_blocks = ((int64_t)E * cap + W - 1) / W;
+        int64_t blocks = T > fill_blocks ? T : fill_blocks;
+        const int64_t resident = resident_blocks(fn, W, sm);
+        if (blocks > resident) blocks = resident;
+        if (blocks < 1) blocks = 1;
+        const uint16_t* xb = static_cast<const uint16_t*>(x);
+        uint8_t* rb = static_cast<uint8_t*>(recv);
+        clear_stale_error();
+#define MOEDC_FUSED_TOKEN_LAUNCH(J)                                                               \
+    launch(moedc::fused_layout_dispatch_token_kernel<J>, (int)blocks, W, sm, stream, xb, topk_idx, \
+           T, H, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, slot, \
+           rb, scales, src_idx, dev_status)
+        if (per_warp == 1)
+            MOEDC_FUSED_TOKEN_LAUNCH(1);
+        else if (per_warp == 2)
+            MOEDC_FUSED_TOKEN_LAUNCH(2);
+        else
+            MOEDC_FUSED_TOKEN_LAUNCH(4);
+#undef MOEDC_FUSED_TOKEN_LAUNCH
+        return launch_status();
+    }
     const int64_t items = (int64_t)T * nslice;
     const bool wide = n > (int64_t)moedc::kFusedNarrow * moedc::kFusedIdsPerThread;
     const int threads = wide ? moedc::kFusedWide : moedc::kFusedNarrow;

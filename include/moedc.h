@@ -305,8 +305,9 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * time.  In between (1024 < T * K <= 65536), with a smaller workspace (at
  * least moedc_layout_workspace_bytes), or when a chunk would exceed 2048
  * entries, layout and dispatch run as two launches (in between that is the
- * faster form).  MOEDC_SCALES_PER_TOKEN always takes the two-launch path (a
- * row's scale needs all of its slices).  Results are identical on every path.
+ * faster form).  With MOEDC_SCALES_PER_TOKEN (a row's scale needs all of
+ * its slices) the single launch gives each block whole tokens, and beyond
+ * 1024 entries layout and dispatch run as two launches.  Results are identical on every path.
  * Test hook: with the environment variable MOEDC_TEST_BARRIER_EXTRA=n set,
  * the cooperative launch's barriers wait for n blocks more than the grid has,
  * so that they run out and report MOEDC_ERR_TIMEOUT; it exists to test that

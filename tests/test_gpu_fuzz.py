@@ -124,8 +124,11 @@ def test_fuzz_token_scale(seed):
     c = synth.make_random_case(**_token_shape(seed))
     d = DevCase(c)
     tok = moedc.FP8_E4M3 | moedc.SCALES_PER_TOKEN
-    lay = run_layout(d)
-    recv, scales, src = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, tok)
+    if seed % 2:   # one call: a single launch up to 1024 entries
+        lay, recv, scales, src = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, tok)
+    else:
+        lay = run_layout(d)
+        recv, scales, src = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, tok)
     deq = moedc.dequant_e4m3(recv, scales, lay.num_tokens_per_expert,
                              scale_layout=moedc.SCALES_PER_TOKEN)
     y = moedc.combine_e4m3(recv, scales, d.topk_idx, lay.slot, d.topk_weights,
@@ -133,6 +136,7 @@ def test_fuzz_token_scale(seed):
     torch.cuda.synchronize()
     ref_lay = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
     ref = oracle.dispatch_token_scale(c.x, c.topk_idx, ref_lay["slot"], c.E, c.cap)
+    compare_layout(lay, ref_lay, c.T)
     np.testing.assert_array_equal(src.cpu().numpy(), ref["src_idx"])
     rows = valid_rows(ref_lay["num_tokens_per_expert"], c.cap)
     if rows.size:

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from combine_moedc_layout_gb300 import moedc, synth
-from parity_util import DevCase, bits_host, compare_combine, run_layout, valid_rows
+from parity_util import DevCase, bits_host, compare_combine, compare_layout, run_layout, valid_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -75,15 +75,18 @@ def test_dispatch_token_scale_parity(name):
     _compare(c, recv, scales, src, ref_lay, ref_d)
 
 
-@pytest.mark.parametrize("name", ["low4", "default_ll", "h640"])
+@pytest.mark.parametrize("name", list(CASES))
 def test_layout_dispatch_token_scale_parity(name):
-    """The one-call entry point takes the two-launch path for per-token scales."""
+    """The one-call entry point: a single launch whose blocks own whole tokens
+    up to 1024 routing entries (low4, low16, default_ll, h12288, h32768,
+    tiny_values: one, two and four slices per warp), layout then dispatch
+    beyond."""
     c = case(name)
     d = DevCase(c)
     lay, recv, scales, src = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, TOK)
     torch.cuda.synchronize()
     ref_lay, ref_d = _oracle(c)
-    np.testing.assert_array_equal(lay.slot.cpu().numpy(), ref_lay["slot"])
+    compare_layout(lay, ref_lay, c.T)
     _compare(c, recv, scales, src, ref_lay, ref_d)
 
 
@@ -122,4 +125,19 @@ def test_token_scale_drops_masks_and_flags_out_of_range():
     ref_lay, ref_d = _oracle(c)
     assert int(lay.status.item()) == oracle.ERR_EXPERT_RANGE
     assert ref_d["status"] == oracle.ERR_EXPERT_RANGE
+    _compare(c, recv, scales, src, ref_lay, ref_d)
+
+
+def test_single_launch_token_scale_drops_masks_and_flags_out_of_range():
+    """The same data errors through the one-call single launch (400 entries)."""
+    c = synth.make_random_case(87, T=100, H=640, K=4, E=8, R=4, cap=None, dtype=synth.FP8_E4M3,
+                               mask_p=0.15)
+    c.cap = max(1, c.cap - 5)
+    c.topk_idx[9, 3] = 11
+    d = DevCase(c)
+    lay, recv, scales, src = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, TOK)
+    torch.cuda.synchronize()
+    ref_lay, ref_d = _oracle(c)
+    assert ref_lay["status"] == oracle.ERR_EXPERT_RANGE
+    compare_layout(lay, ref_lay, c.T)
     _compare(c, recv, scales, src, ref_lay, ref_d)
