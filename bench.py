@@ -145,18 +145,28 @@ def ncu_traffic(kernel: str):
     ent = d.get(kernel)
     if not ent:
         return None
-    if ent.get("source_sha256") != source_hash():
+    if ent.get("source_sha256") != source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_full_launch")
 
 
-def source_hash() -> str:
+# the sources each measured kernel is compiled from (its own file, the shared
+# device helpers and the public header); traffic counters stay valid while
+# these are unchanged
+KERNEL_SOURCES = {
+    "dispatch_kernel": ["csrc/dispatch.cu", "csrc/dispatch_item.cuh", "csrc/common.cuh"],
+    "combine_kernel": ["csrc/combine.cu", "csrc/common.cuh"],
+}
+
+
+def source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "combine_moedc_layout_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    pkg = os.path.join(ROOT, "combine_moedc_layout_gb300")
+    files = [os.path.join(pkg, f) for f in KERNEL_SOURCES[kernel]]
+    files.append(os.path.join(ROOT, "include", "moedc.h"))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
     return h.hexdigest()
 
 
