@@ -10,9 +10,11 @@
  *  cap slots per expert, G = H / 128 FP8 scale groups.
  *
  *  Every pointer is a DEVICE pointer owned by the caller.  The library never
- *  allocates, frees or synchronises, keeps no state between calls and reads
- *  no environment variable.  Calls are asynchronous on `stream` (0 = the
- *  legacy default stream) and contain no host-side reads of device data.
+ *  allocates, frees or synchronises.  Between calls it keeps only host-side
+ *  caches (device attributes, occupancy) and a launch counter; the one
+ *  environment variable it reads is a test hook of moedc_layout_dispatch.
+ *  Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *  contain no host-side reads of device data.
  *
  *  Row-major layouts:
  *    x, y                 bf16   [T, H]
@@ -23,7 +25,8 @@
  *    num_tokens_per_rank  int32  [R]
  *    is_token_in_rank     uint8  [T, R]   0 / 1
  *    recv, expert_out     bf16 or e4m3 [E, cap, H]   (expert-major)
- *    scales               fp32   [E, cap, G]
+ *    scales               fp32   [E, cap, G]  ([E, G, cap] or [E, cap] with
+ *                                               the scale-layout flags below)
  *    src_idx              int32  [E, cap]
  *  x, y, recv and expert_out must be 16-byte aligned; the others 4-byte
  *  aligned (is_token_in_rank: any alignment).
@@ -120,12 +123,12 @@ MOEDC_EXPORT int moedc_api_version(void);
 MOEDC_EXPORT const char* moedc_strerror(int code);
 
 /*
- * Bytes of device scratch that moedc_layout / moedc_layout_dispatch need for
- * this shape (0 when T * K <= 65536: that layout is one launch without
- * scratch).  The caller
- * allocates it (any 16-byte aligned device buffer of at least this size) and
- * may reuse it across calls that are ordered on one stream.  Returns 0 for
- * arguments that the layout would reject.
+ * Bytes of device scratch that moedc_layout needs for this shape (0 when
+ * T * K <= 65536: that layout is one launch without scratch); also enough for
+ * moedc_layout_dispatch to run as layout then dispatch.  The caller allocates
+ * it (any 16-byte aligned device buffer of at least this size) and may reuse
+ * it across calls that are ordered on one stream.  Returns 0 for arguments
+ * that the layout would reject.
  */
 MOEDC_EXPORT size_t moedc_layout_workspace_bytes(int T, int K, int E, int R);
 
@@ -293,21 +296,27 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * and each layout output is written by the warp that owns it (a token's slots
  * and rank flags by the warp copying its first slice, a rank's count by one
  * warp, the expert counts by block 0).
- * Inputs beyond the single-launch layout (T * K > 65536, where
- * moedc_layout_workspace_bytes is nonzero) with a workspace of at least
- * moedc_layout_dispatch_workspace_bytes(T, K, E, R) bytes are also ONE launch,
- * a cooperative one [UCCL749 per-expert counts a rank waits on]: each block
- * ranks and counts a contiguous chunk of tokens, a grid barrier, one block
- * per expert / rank scans the chunks' counts, a second barrier, then each
- * block assigns its chunk's slots and copies its chunk.  The barriers are
- * bounded waits (MOEDC_ERR_TIMEOUT when one runs out); the workspace needs
- * no initialisation but must not be shared by calls that can run at the same
- * time.  In between (1024 < T * K <= 65536), with a smaller workspace (at
- * least moedc_layout_workspace_bytes), or when a chunk would exceed 2048
- * entries, layout and dispatch run as two launches (in between that is the
- * faster form).  With MOEDC_SCALES_PER_TOKEN (a row's scale needs all of
- * its slices) the single launch gives each block whole tokens, and beyond
- * 1024 entries layout and dispatch run as two launches.  Results are identical on every path.
+ * With MOEDC_SCALES_PER_TOKEN (a row's scale needs all of its slices) the
+ * single launch gives each block whole tokens instead.
+ *
+ * Beyond the single-launch layout (T * K > 65536, where
+ * moedc_layout_workspace_bytes is nonzero), with a workspace of at least
+ * moedc_layout_dispatch_workspace_bytes(T, K, E, R) bytes, it is also ONE
+ * launch, a cooperative one [UCCL749 per-expert counts a rank waits on]:
+ * each block ranks and counts a contiguous chunk of tokens; a grid barrier;
+ * one block per expert / rank scans the chunks' counts; a second barrier;
+ * then each block assigns its chunk's slots and copies its chunk.  The
+ * barriers are bounded waits (MOEDC_ERR_TIMEOUT when one runs out).  The
+ * workspace needs no initialisation but must not be shared by calls that can
+ * run at the same time.
+ *
+ * Everything else runs as moedc_layout then moedc_dispatch: 1024 < T * K <=
+ * 65536 (where that is the faster form), a workspace smaller than
+ * moedc_layout_dispatch_workspace_bytes (it must still hold
+ * moedc_layout_workspace_bytes), a chunk that would exceed 2048 entries, and
+ * MOEDC_SCALES_PER_TOKEN beyond 1024 entries.  Results are identical on every
+ * path.
+ *
  * Test hook: with the environment variable MOEDC_TEST_BARRIER_EXTRA=n set,
  * the cooperative launch's barriers wait for n blocks more than the grid has,
  * so that they run out and report MOEDC_ERR_TIMEOUT; it exists to test that
