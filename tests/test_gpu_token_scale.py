@@ -141,3 +141,23 @@ def test_single_launch_token_scale_drops_masks_and_flags_out_of_range():
     assert ref_lay["status"] == oracle.ERR_EXPERT_RANGE
     compare_layout(lay, ref_lay, c.T)
     _compare(c, recv, scales, src, ref_lay, ref_d)
+
+
+@pytest.mark.parametrize("one_call", [False, True])
+def test_token_scale_empty_and_all_masked(one_call):
+    """T = 0, and every entry masked: nothing is written but src_idx = -1
+    everywhere and zero counts; no data error."""
+    for T, mask in ((0, 0.0), (37, 1.0)):
+        c = synth.make_random_case(88, T=T, H=384, K=4, E=8, R=2, cap=5, dtype=synth.FP8_E4M3,
+                                   mask_p=mask)
+        d = DevCase(c)
+        if one_call:
+            lay, recv, scales, src = moedc.layout_dispatch(d.x, d.topk_idx, c.E, c.R, c.cap, TOK)
+        else:
+            lay = run_layout(d)
+            recv, scales, src = moedc.dispatch(d.x, d.topk_idx, lay, c.E, c.cap, TOK)
+        torch.cuda.synchronize()
+        assert int(lay.status.item()) == 0
+        assert (lay.num_tokens_per_expert.cpu().numpy() == 0).all()
+        assert (lay.num_tokens_per_rank.cpu().numpy() == 0).all()
+        assert (src.cpu().numpy() == -1).all()
