@@ -190,3 +190,26 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(root, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "moedc_oracle" not in src, f
+
+
+def _build_c_caller(tmp_path):
+    """Compile tests/capi/moe_round.c as C11 against include/moedc.h and link it
+    to libmoedc.so and the CUDA runtime; returns the executable's path."""
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = str(tmp_path / "moe_round")
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+           "-I" + os.path.join(ROOT, "include"), "-I" + os.path.join(cuda, "include"),
+           os.path.join(ROOT, "tests", "capi", "moe_round.c"), "-o", exe,
+           "-L" + os.path.dirname(mbuild.LIB_PATH), "-lmoedc",
+           "-L" + os.path.join(cuda, "lib64"), "-lcudart",
+           "-Wl,-rpath," + os.path.dirname(mbuild.LIB_PATH)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    return exe
+
+
+def test_plain_c_caller_compiles_and_links(lib, tmp_path):
+    """The header is valid C11 and a C program links against the library
+    with no C++ or Python in between (running it needs a GPU: see
+    test_gpu_capi_c.py)."""
+    assert os.path.exists(_build_c_caller(tmp_path))
