@@ -157,3 +157,19 @@ def test_combine_e4m3_per_token_k1_unit_weight_equals_dequant():
     deq = oracle.dequant_e4m3_token(d["recv"], d["scales"], lay["num_tokens_per_expert"])
     for t in range(c.T):
         np.testing.assert_array_equal(y[t], deq[c.topk_idx[t, 0], lay["slot"][t, 0]])
+
+
+def test_hand_worked_row():
+    """One row whose maximum is 7, so s = 7 / 448 = 2^-6 exactly and every
+    quotient x / s is exact; the codes follow from the e4m3fn grid by hand:
+    448 -> 0x7E; -224 = -1.75 * 2^7 -> 0xF6; 112 = 1.75 * 2^6 -> 0x6E;
+    28 = 1.75 * 2^4 -> 0x5E; bf16(0.1) / s = 6.40625 lies between 6.0 and 6.5
+    (spacing 0.5 in [4, 8)) and rounds to 6.5 = 1.625 * 2^2 -> 0x4D;
+    bf16(1e-4) / s = 0.0064087 is 3.28 subnormal steps of 2^-9 -> 0x03; 0 -> 0x00."""
+    vals = np.zeros(128, np.float32)
+    vals[:7] = [7.0, -3.5, 1.75, 0.4375, 0.1, 1e-4, 0.0]
+    x = synth.f32_to_bf16_bits(vals).reshape(1, 128)
+    d = oracle.dispatch_token_scale(x, np.array([[0]], np.int32), np.array([[0]], np.int32), 1, 1)
+    assert d["scales"][0, 0] == np.float32(2.0**-6)
+    assert [int(v) for v in d["recv"][0, 0, :7]] == [0x7E, 0xF6, 0x6E, 0x5E, 0x4D, 0x03, 0x00]
+    assert (d["recv"][0, 0, 7:] == 0).all()
