@@ -252,6 +252,103 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
 }
 
+// K <= 8: a warp owns half of a token's 512-channel slices; the routing of
+// its rows (row offset, weight, scale base) is derived once and kept in
+// registers across those slices.  Each row's shuffles, 64-bit address
+// arithmetic and scale-index work were otherwise redone for every slice; with
+// 4.5 instructions per element per term the kernel is bound by issue, and
+// hoisting them took the 4096-token workload from 75.8 to 59.4 us.
+constexpr int kHalves = 2;   // measured: 1 part 63.5 us, 2 parts 59.4, 3 parts 60.4, 4 parts 68.6
+__global__ void __launch_bounds__(kCombineThreads, 2)
+combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __restrict__ scales,
+                         int scale_mode, int E, int cap, int H,
+                         const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
+                         const float* __restrict__ topk_weights, int T, int K,
+                         uint16_t* __restrict__ y, int32_t* __restrict__ status)
+{
+    pdl_enter();
+    const int lane = threadIdx.x % kWarp;
+    const int G = H / 128;
+    const int nslice = (H + 511) / 512;
+    const int per_half = (nslice + kHalves - 1) / kHalves;
+    const int items = T * kHalves;
+    const int nwarps = gridDim.x * (blockDim.x / kWarp);
+    bool bad = false;
+    for (int item = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp; item < items;
+         item += nwarps) {
+        const int t = item / kHalves;
+        const int half = item - t * kHalves;
+        int my_e = -1, my_s = -1;
+        float my_w = 0.0f;
+        if (lane < K) {
+            my_e = __ldg(topk_idx + (int64_t)t * K + lane);
+            my_s = __ldg(slot + (int64_t)t * K + lane);
+            my_w = __ldg(topk_weights + (int64_t)t * K + lane);
+            if (half == 0 && (my_e < -1 || my_e >= E)) bad = true;
+        }
+        int64_t roff[kCombine8Batch];
+        int64_t sbase[kCombine8Batch];
+        int64_t sstep;   // scale index step per 128-channel group
+        float wk[kCombine8Batch];
+        unsigned okm = 0;
+#pragma unroll
+        for (int j = 0; j < kCombine8Batch; ++j) {
+            const int e = __shfl_sync(0xffffffffu, my_e, j);
+            const int sidx = __shfl_sync(0xffffffffu, my_s, j);
+            wk[j] = __shfl_sync(0xffffffffu, my_w, j);
+            const bool ok = j < K && e >= 0 && e < E && sidx >= 0 && sidx < cap;
+            okm |= (ok ? 1u : 0u) << j;
+            const int64_t row = ok ? (int64_t)e * cap + sidx : 0;
+            roff[j] = row * H;
+            sbase[j] = !ok ? 0 : scale_mode == 2 ? row
+                         : scale_mode == 1 ? (int64_t)e * G * cap + sidx : row * G;
+        }
+        sstep = scale_mode == 2 ? 0 : scale_mode == 1 ? cap : 1;
+        const int sl_end = min(nslice, (half + 1) * per_half);
+        for (int sl = half * per_half; sl < sl_end; ++sl) {
+            const int c0 = sl * 512 + lane * 16;
+            const bool act = c0 < H;
+            const int g = act ? c0 / 128 : 0;
+            uint4 q[kCombine8Batch];
+            float sc[kCombine8Batch];
+#pragma unroll
+            for (int j = 0; j < kCombine8Batch; ++j) {
+                q[j] = ld_global_nc(reinterpret_cast<const uint4*>(expert_out + roff[j] +
+                                                                    (act ? c0 : 0)));
+                sc[j] = __ldg(scales + (((okm >> j) & 1u) ? sbase[j] + g * sstep : 0));
+            }
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kCombine8Batch; ++j) {
+                if (!((okm >> j) & 1u)) continue;
+                const uint32_t u[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a, b, c, d;
+                    e4m3x2_to_f32(u[i] & 0xffffu, a, b);
+                    e4m3x2_to_f32(u[i] >> 16, c, d);
+                    acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(wk[j], __fmul_rn(a, sc[j])));
+                    acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(wk[j], __fmul_rn(b, sc[j])));
+                    acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(wk[j], __fmul_rn(c, sc[j])));
+                    acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(wk[j], __fmul_rn(d, sc[j])));
+                }
+            }
+            if (act) {
+                uint16_t* dst = y + (int64_t)t * H + c0;
+                st_global_cs(reinterpret_cast<uint4*>(dst),
+                             make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+                st_global_cs(reinterpret_cast<uint4*>(dst + 8),
+                             make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                        pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+            }
+        }
+    }
+    if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
+}
+
 }  // namespace moedc
 
 extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_scales,
@@ -275,6 +372,19 @@ extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_sc
         !aligned(dev_status, 4))
         return MOEDC_ERR_ARG;
     if (T == 0) return MOEDC_OK;
+    if (K <= moedc::kCombine8Batch) {
+        const int64_t items = (int64_t)T * moedc::kHalves;
+        int64_t blocks = (items + moedc::kCombineThreads / moedc::kWarp - 1) /
+                         (moedc::kCombineThreads / moedc::kWarp);
+        const int64_t resident = resident_blocks((const void*)moedc::combine_e4m3_rows_kernel,
+                                                 moedc::kCombineThreads, 0);
+        if (blocks > resident) blocks = resident;
+        clear_stale_error();
+        launch(moedc::combine_e4m3_rows_kernel, (int)blocks, moedc::kCombineThreads, 0, stream,
+               static_cast<const uint8_t*>(expert_out), expert_scales, mode, E, cap, H, topk_idx,
+               slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status);
+        return launch_status();
+    }
     const int64_t items = (int64_t)T * ((H + 511) / 512);
     int64_t blocks = (items + moedc::kCombineThreads / moedc::kWarp - 1) /
                      (moedc::kCombineThreads / moedc::kWarp);
