@@ -25,17 +25,21 @@ int sm_count()
 int resident_blocks(const void* kernel, int threads, size_t smem)
 {
     // blocks of `kernel` that fit on the whole device at once (occupancy x
-    // SMs), cached per kernel and device; grid-strided kernels launch at most
-    // this many so that no block waits for a second wave
+    // SMs), cached per kernel, block size, shared-memory size and device;
+    // grid-strided kernels launch at most this many so that no block waits
+    // for a second wave.  The single-launch kernels' shared memory follows the
+    // batch shape, so a serving loop meets many keys: the table keeps the most
+    // recent ones (round-robin replacement once full).
     struct Entry {
         const void* kernel;
         int dev, threads;
         size_t smem;
         int blocks;
     };
+    constexpr int kEntries = 256;
     static std::mutex mu;
-    static Entry cache[64];
-    static int used = 0;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     std::lock_guard<std::mutex> lock(mu);
@@ -48,7 +52,9 @@ int resident_blocks(const void* kernel, int threads, size_t smem)
             cudaSuccess || per_sm < 1)
         per_sm = 1;
     const int blocks = per_sm * sm_count();
-    if (used < 64) cache[used++] = Entry{kernel, dev, threads, smem, blocks};
+    cache[next] = Entry{kernel, dev, threads, smem, blocks};
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
     return blocks;
 }
 
