@@ -70,9 +70,9 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
             c[v] = sl * kCombineSlice + v * 256 + lane * 8;
             act[v] = c[v] < H;
         }
-        float acc[8 * kCombineVec];
+        float2 acc[4 * kCombineVec];   // channel pairs
 #pragma unroll
-        for (int i = 0; i < 8 * kCombineVec; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 4 * kCombineVec; ++i) acc[i] = make_float2(0.0f, 0.0f);
         int nx_e, nx_s;
         float nx_w;
 
@@ -101,15 +101,13 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
 #pragma unroll
             for (int j = 0; j < kCombineBatch; ++j) {
                 if (!ok[j]) continue;
+                const float2 w2 = splat2(wk[j]);
 #pragma unroll
                 for (int v = 0; v < kCombineVec; ++v) {
                     const uint32_t u[4] = {buf[j][v].x, buf[j][v].y, buf[j][v].z, buf[j][v].w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float* a = acc + 8 * v + 2 * i;
-                        a[0] = __fadd_rn(a[0], __fmul_rn(wk[j], bf16_lo(u[i])));
-                        a[1] = __fadd_rn(a[1], __fmul_rn(wk[j], bf16_hi(u[i])));
-                    }
+                    for (int i = 0; i < 4; ++i)   // acc + w * x, each rounded, never fused
+                        acc[4 * v + i] = add2_rn(acc[4 * v + i], mul2_rn(w2, bf16x2_to_f32x2(u[i])));
                 }
             }
         }
@@ -117,10 +115,10 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
 #pragma unroll
         for (int v = 0; v < kCombineVec; ++v) {
             if (!act[v]) continue;
-            const float* a = acc + 8 * v;
+            const float2* a = acc + 4 * v;
             st_global_cs(reinterpret_cast<uint4*>(yrow + c[v]),
-                         make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                                    pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7])));
+                         make_uint4(pack_bf16x2(a[0]), pack_bf16x2(a[1]), pack_bf16x2(a[2]),
+                                    pack_bf16x2(a[3])));
         }
         my_e = nx_e;
         my_s = nx_s;
@@ -193,9 +191,9 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
         const int c0 = sl * 512 + lane * 16;
         const bool act = c0 < H;
         const int g = act ? c0 / 128 : 0;
-        float acc[16];
+        float2 acc[8];   // channel pairs
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
         for (int k0 = 0; k0 < K; k0 += kCombine8Batch) {
             uint4 q[kCombine8Batch];
             float sc[kCombine8Batch], wk[kCombine8Batch];
@@ -221,26 +219,25 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
             for (int j = 0; j < kCombine8Batch; ++j) {
                 if (!ok[j]) continue;
                 const uint32_t u[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+                const float2 w2 = splat2(wk[j]), s2 = splat2(sc[j]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    float a, b, c, d;
-                    e4m3x2_to_f32(u[i] & 0xffffu, a, b);
-                    e4m3x2_to_f32(u[i] >> 16, c, d);
-                    acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(wk[j], __fmul_rn(a, sc[j])));
-                    acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(wk[j], __fmul_rn(b, sc[j])));
-                    acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(wk[j], __fmul_rn(c, sc[j])));
-                    acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(wk[j], __fmul_rn(d, sc[j])));
+                    // acc + w * (q * s), each operation rounded, never fused
+                    const float2 lo = mul2_rn(e4m3x2_to_f32x2(u[i] & 0xffffu), s2);
+                    const float2 hi = mul2_rn(e4m3x2_to_f32x2(u[i] >> 16), s2);
+                    acc[2 * i] = add2_rn(acc[2 * i], mul2_rn(w2, lo));
+                    acc[2 * i + 1] = add2_rn(acc[2 * i + 1], mul2_rn(w2, hi));
                 }
             }
         }
         if (act) {
             uint16_t* dst = y + (int64_t)t * H + c0;
             st_global_cs(reinterpret_cast<uint4*>(dst),
-                         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+                         make_uint4(pack_bf16x2(acc[0]), pack_bf16x2(acc[1]), pack_bf16x2(acc[2]),
+                                    pack_bf16x2(acc[3])));
             st_global_cs(reinterpret_cast<uint4*>(dst + 8),
-                         make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                    pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+                         make_uint4(pack_bf16x2(acc[4]), pack_bf16x2(acc[5]), pack_bf16x2(acc[6]),
+                                    pack_bf16x2(acc[7])));
         }
         t += dt;
         sl += dsl;
@@ -317,32 +314,31 @@ combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __
                                                                     (act ? c0 : 0)));
                 sc[j] = __ldg(scales + (((okm >> j) & 1u) ? sbase[j] + g * sstep : 0));
             }
-            float acc[16];
+            float2 acc[8];   // channel pairs
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int j = 0; j < kCombine8Batch; ++j) {
                 if (!((okm >> j) & 1u)) continue;
                 const uint32_t u[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+                const float2 w2 = splat2(wk[j]), s2 = splat2(sc[j]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    float a, b, c, d;
-                    e4m3x2_to_f32(u[i] & 0xffffu, a, b);
-                    e4m3x2_to_f32(u[i] >> 16, c, d);
-                    acc[4 * i + 0] = __fadd_rn(acc[4 * i + 0], __fmul_rn(wk[j], __fmul_rn(a, sc[j])));
-                    acc[4 * i + 1] = __fadd_rn(acc[4 * i + 1], __fmul_rn(wk[j], __fmul_rn(b, sc[j])));
-                    acc[4 * i + 2] = __fadd_rn(acc[4 * i + 2], __fmul_rn(wk[j], __fmul_rn(c, sc[j])));
-                    acc[4 * i + 3] = __fadd_rn(acc[4 * i + 3], __fmul_rn(wk[j], __fmul_rn(d, sc[j])));
+                    // acc + w * (q * s), each operation rounded, never fused
+                    const float2 lo = mul2_rn(e4m3x2_to_f32x2(u[i] & 0xffffu), s2);
+                    const float2 hi = mul2_rn(e4m3x2_to_f32x2(u[i] >> 16), s2);
+                    acc[2 * i] = add2_rn(acc[2 * i], mul2_rn(w2, lo));
+                    acc[2 * i + 1] = add2_rn(acc[2 * i + 1], mul2_rn(w2, hi));
                 }
             }
             if (act) {
                 uint16_t* dst = y + (int64_t)t * H + c0;
                 st_global_cs(reinterpret_cast<uint4*>(dst),
-                             make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+                             make_uint4(pack_bf16x2(acc[0]), pack_bf16x2(acc[1]),
+                                        pack_bf16x2(acc[2]), pack_bf16x2(acc[3])));
                 st_global_cs(reinterpret_cast<uint4*>(dst + 8),
-                             make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                        pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+                             make_uint4(pack_bf16x2(acc[4]), pack_bf16x2(acc[5]),
+                                        pack_bf16x2(acc[6]), pack_bf16x2(acc[7])));
             }
         }
     }

@@ -82,16 +82,13 @@ dequant_e4m3_kernel(const uint8_t* __restrict__ recv, const float* __restrict__ 
         const int64_t si = scale_mode == 2   ? row                                   // per row
                            : scale_mode == 1 ? ((int64_t)lo * G + g) * cap + sidx    // [E][G][cap]
                                              : row * G + g;                          // [E][cap][G]
-        const float sc = __ldg(scales + si);
+        const float2 s2 = splat2(__ldg(scales + si));
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float a, b, c, d;
-            e4m3x2_to_f32(w[i] & 0xffffu, a, b);
-            e4m3x2_to_f32(w[i] >> 16, c, d);
-            o[2 * i] = pack_bf16x2(__fmul_rn(a, sc), __fmul_rn(b, sc));
-            o[2 * i + 1] = pack_bf16x2(__fmul_rn(c, sc), __fmul_rn(d, sc));
+        for (int i = 0; i < 4; ++i) {   // RN(q * s), then the bf16 nearest-even rounding
+            o[2 * i] = pack_bf16x2(mul2_rn(e4m3x2_to_f32x2(w[i] & 0xffffu), s2));
+            o[2 * i + 1] = pack_bf16x2(mul2_rn(e4m3x2_to_f32x2(w[i] >> 16), s2));
         }
         uint16_t* dst = out + row * H + c0;
         st_global_cs(reinterpret_cast<uint4*>(dst), make_uint4(o[0], o[1], o[2], o[3]));

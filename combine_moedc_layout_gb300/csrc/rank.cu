@@ -134,9 +134,9 @@ rank_combine_kernel(const uint16_t* __restrict__ rank_out, int R, int cap_rank, 
         const int c0 = cur.sl * 512 + lane * 8;
         const int c1 = c0 + 256;
         const bool a0 = c0 < H, a1 = c1 < H;
-        float acc[16];
+        float2 acc[8];   // channel pairs
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
         for (int r0 = 0; r0 < R; r0 += kWarp) {
             int my_row = -1;
             if (r0 + lane < R) {
@@ -167,8 +167,7 @@ rank_combine_kernel(const uint16_t* __restrict__ rank_out, int R, int cap_rank, 
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (i >= 4 && !a1) break;
-                        acc[2 * i] = __fadd_rn(acc[2 * i], bf16_lo(u[i]));
-                        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], bf16_hi(u[i]));
+                        acc[i] = add2_rn_unfed(acc[i], bf16x2_to_f32x2(u[i]));
                     }
                 }
             }
@@ -176,13 +175,12 @@ rank_combine_kernel(const uint16_t* __restrict__ rank_out, int R, int cap_rank, 
         uint16_t* yrow = y + (int64_t)cur.t * H;
         if (a0)
             st_global_cs(reinterpret_cast<uint4*>(yrow + c0),
-                         make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+                         make_uint4(pack_bf16x2(acc[0]), pack_bf16x2(acc[1]), pack_bf16x2(acc[2]),
+                                    pack_bf16x2(acc[3])));
         if (a1)
             st_global_cs(reinterpret_cast<uint4*>(yrow + c1),
-                         make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                    pack_bf16x2(acc[12], acc[13]),
-                                    pack_bf16x2(acc[14], acc[15])));
+                         make_uint4(pack_bf16x2(acc[4]), pack_bf16x2(acc[5]), pack_bf16x2(acc[6]),
+                                    pack_bf16x2(acc[7])));
     }
 }
 
