@@ -52,11 +52,15 @@ def algorithmic_bytes(T, H, K, E, R, cap, N, fp8):
     return dict(layout=layout, dispatch=dispatch, combine=combine)
 
 
-def workload_config(c):
+def workload_config(c, n_gpus: int = 1):
+    """The workload both arms run (identical keys and values in both lines)."""
     return {"workload": f"{c.name}: T={c.T} H={c.H} K={c.K} E={c.E} R={c.R} cap={c.cap} "
                         "fp8 e4m3 dispatch (per-128 fp32 scales), bf16 combine, uniform routing",
             "T": c.T, "H": c.H, "K": c.K, "E": c.E, "R": c.R, "cap": c.cap,
-            "dispatch_dtype": "e4m3", "combine_dtype": "bf16", "seed": c.seed}
+            "dispatch_dtype": "e4m3", "combine_dtype": "bf16", "seed": c.seed,
+            "parallelism": f"replicas x{n_gpus}",
+            "l2": "inputs larger than L2: ~0.9 GB of HBM touched per step vs 129 MB L2, no flush "
+                  "between steps; the isolated per-kernel times read 1 GiB before each call"}
 
 
 # ---------------------------------------------------------------- clocks
@@ -173,67 +177,179 @@ def source_hash(kernel: str) -> str:
 # ------------------------------------------------------------ CPU oracle
 
 
-def oracle_step(c, T_s: int):
+def _token_chunks(T_s: int, n: int) -> list[tuple[int, int]]:
+    n = max(1, min(n, T_s))
+    return [(T_s * j // n, T_s * (j + 1) // n) for j in range(n)]
+
+
+def oracle_step(c, T_s: int, threads: int = 1, pool=None, keep: bool = False):
     """One oracle pass (layout, fp8 dispatch, combine) over the first T_s
-    tokens of the workload; returns (seconds, algorithmic bytes)."""
+    tokens of the workload; returns (seconds, algorithmic bytes, outputs or
+    None).
+
+    threads > 1 splits the tokens of dispatch and combine into contiguous
+    runs, one oracle call per run on a thread of `pool` (the oracle's ctypes
+    calls release the GIL).  The layout stays one call: its slots are a scan
+    in token order.  The oracle functions are the same ones either way."""
     import oracle
     from combine_moedc_layout_gb300 import synth
 
+    fp8 = c.dtype == synth.FP8_E4M3
     idx = np.ascontiguousarray(c.topk_idx[:T_s])
     x = np.ascontiguousarray(c.x[:T_s])
     w = np.ascontiguousarray(c.topk_weights[:T_s])
     eo = c.extra["eo_host"]
     t0 = time.perf_counter()
     lay = oracle.layout(idx, c.E, c.R, c.cap)
-    oracle.dispatch(x, idx, lay["slot"], c.E, c.cap, fp8=c.dtype == synth.FP8_E4M3)
-    oracle.combine(eo, idx, lay["slot"], w)
+    sl = lay["slot"]
+    if threads <= 1:
+        d = oracle.dispatch(x, idx, sl, c.E, c.cap, fp8=fp8)
+        y = oracle.combine(eo, idx, sl, w)["y"]
+        parts = None
+    else:
+        recv = np.zeros((c.E, c.cap, c.H), np.uint8 if fp8 else np.uint16)
+
+        def run(ab):
+            lo, hi = ab
+            dd = oracle.dispatch(x[lo:hi], idx[lo:hi], sl[lo:hi], c.E, c.cap, fp8=fp8,
+                                 recv=recv)
+            yy = oracle.combine(eo, idx[lo:hi], sl[lo:hi], w[lo:hi])["y"]
+            return lo, dd, yy
+
+        parts = list(pool.map(run, _token_chunks(T_s, threads)))
     dt = time.perf_counter() - t0
     N = int(((idx >= 0) & (idx < c.E)).sum())
-    b = algorithmic_bytes(T_s, c.H, c.K, c.E, c.R, c.cap, N, c.dtype == synth.FP8_E4M3)
-    return dt, sum(b.values())
+    b = algorithmic_bytes(T_s, c.H, c.K, c.E, c.R, c.cap, N, fp8)
+    out = None
+    if keep:
+        if parts is None:
+            out = dict(layout=lay, recv=d["recv"], scales=d["scales"], src_idx=d["src_idx"], y=y)
+        else:
+            G = c.H // 128
+            scales = np.zeros((c.E, c.cap, G), np.float32) if fp8 else None
+            src_idx = np.full((c.E, c.cap), -1, np.int32)
+            for lo, dd, _ in parts:
+                filled = dd["src_idx"] >= 0
+                src_idx[filled] = dd["src_idx"][filled] + lo
+                if fp8:
+                    scales[filled] = dd["scales"][filled]
+            out = dict(layout=lay, recv=recv, scales=scales, src_idx=src_idx,
+                       y=np.concatenate([yy for _, _, yy in parts], axis=0))
+    return dt, sum(b.values()), out
+
+
+def same_oracle_outputs(a: dict, b: dict) -> bool:
+    """Bit equality of two oracle_step outputs (single- vs multi-threaded)."""
+    for k in ("recv", "src_idx", "y"):
+        if not np.array_equal(a[k], b[k]):
+            return False
+    if (a["scales"] is None) != (b["scales"] is None):
+        return False
+    if a["scales"] is not None and not np.array_equal(a["scales"].view(np.uint32),
+                                                      b["scales"].view(np.uint32)):
+        return False
+    return True
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def cpu_model() -> str:
+    """The host CPU's model name as lscpu prints it ("Model name"); x86
+    /proc/cpuinfo carries it as "model name"; Arm kernels give only the
+    implementer / part codes, reported as such when lscpu is missing."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10,
+                           env=dict(os.environ, LC_ALL="C"))
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    fields = {}
     try:
         for line in open("/proc/cpuinfo"):
-            if line.lower().startswith(("model name", "cpu part")):
-                return line.split(":", 1)[1].strip()
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip().lower(), v.strip())
     except OSError:
         pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        return f"Arm CPU implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
     import platform
     return platform.machine()
 
 
+def cpu_baseline_full(c) -> dict:
+    """The oracle timed on one full step of the workload: once on one core,
+    once with the tokens split over every host core; the two runs' outputs
+    must be bit-identical."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    n = host_cores()
+    dt1, b, out1 = oracle_step(c, c.T, keep=True)
+    with ThreadPoolExecutor(max_workers=n) as pool:
+        oracle_step(c, min(c.T, 4 * n), threads=n, pool=pool)     # warm the pool
+        dtn, _, outn = oracle_step(c, c.T, threads=n, pool=pool, keep=True)
+    if not same_oracle_outputs(out1, outn):
+        raise RuntimeError("the multi-threaded oracle step differs from the single-threaded one")
+    model = cpu_model()
+    return {"value": b / dtn / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "seconds": dtn, "nproc": n, "cpu_model": model,
+            "single_core": {"value": b / dt1 / 1e9, "seconds": dt1, "cores": 1},
+            "sample": f"one full step of the workload (all {c.T} tokens): layout, fp8 dispatch, "
+                      f"combine; plain-C oracle, dispatch and combine split by token runs over "
+                      f"{n} threads (outputs bit-identical to the single-core run); {model}"}
+
+
 def run_reference(args, rank: int) -> None:
+    """The oracle as the reference arm: the same workload, on every host core
+    of rank 0 (tokens split over threads for dispatch and combine), each step
+    a token sample sized so that the run stays within about two minutes."""
     if rank != 0:
         return
+    from concurrent.futures import ThreadPoolExecutor
+
     from combine_moedc_layout_gb300 import synth
     import oracle
     oracle.build()
     c = synth.make_case(WORKLOAD)
     c.extra["eo_host"] = synth.make_expert_out(c, 0)
+    n = host_cores()
     budget_s = 120.0
-    dt, _ = oracle_step(c, 32)                      # calibration, not timed
-    per_tok = dt / 32
-    T_s = int(max(1, min(c.T, budget_s / (args.steps + args.warmup) / per_tok)))
-    for _ in range(args.warmup):
-        oracle_step(c, T_s)
-    tot_t = 0.0
-    tot_b = 0
-    for _ in range(args.steps):
-        dt, b = oracle_step(c, T_s)
-        tot_t += dt
-        tot_b += b
+    with ThreadPoolExecutor(max_workers=n) as pool:
+        T_cal = min(c.T, 32 * n)
+        dt, _, _ = oracle_step(c, T_cal, threads=n, pool=pool)     # calibration, not timed
+        per_tok = dt / T_cal
+        T_s = int(max(1, min(c.T, budget_s / (args.steps + args.warmup) / per_tok)))
+        for _ in range(args.warmup):
+            oracle_step(c, T_s, threads=n, pool=pool)
+        tot_t = 0.0
+        tot_b = 0
+        for _ in range(args.steps):
+            dt, b, _ = oracle_step(c, T_s, threads=n, pool=pool)
+            tot_t += dt
+            tot_b += b
     value = tot_b / tot_t / 1e9
+    model = cpu_model()
     sample = (f"first {T_s} of {c.T} tokens of the workload per step (same H, K, E, R, cap); "
-              f"single-threaded plain-C oracle; {cpu_model()}")
+              f"plain-C oracle, dispatch and combine split by token runs over {n} threads; "
+              f"{model}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/bf16 (fp32 arithmetic)",
-            "data": "synthetic", "config": workload_config(c),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 dispatch / bf16 combine (fp32 arithmetic)",
+            "data": "synthetic (seeded numpy: x~N(0,1) bf16, uniform distinct top-8)",
+            "config": workload_config(c, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle",
+                             "nproc": n, "cpu_model": model, "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -556,6 +672,41 @@ def side_workloads(dev) -> dict:
     return out
 
 
+def isolated_kernels(dev, stream, calls: dict, nbytes: dict, reps: int = 400,
+                     warm: int = 20) -> dict:
+    """Each kernel timed alone: before every timed call a 1 GiB read evicts
+    L2 (and writes back whatever the previous call left dirty, outside the
+    timed region), then CUDA events on the launching stream bracket the one
+    call.  `reps` timed calls after `warm` untimed ones, whatever --steps is;
+    median, p10 and p90."""
+    import torch
+
+    flush = torch.ones(256 << 20, dtype=torch.float32, device=dev)
+    peak, _ = hbm_peak()
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(warm):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        sink = []
+        for a, b in ev:
+            sink.append(flush.sum())
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        med = us[len(us) // 2]
+        gbs = nbytes[name] / (med * 1e-6) / 1e9
+        out[name] = {"us_median": med, "us_p10": us[len(us) // 10],
+                     "us_p90": us[(9 * len(us)) // 10], "reps": reps,
+                     "algorithmic_bytes": nbytes[name], "gbs": gbs,
+                     "frac_of_measured_peak": gbs / peak, "frac_of_8tbs": gbs / HBM_NOMINAL_GBS}
+    del flush
+    return out
+
+
 def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     import torch
 
@@ -643,14 +794,46 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         torch.distributed.barrier()
     # per-kernel durations: a second pass of the same steps with an event
     # between every two kernels (these include the bubbles the events add)
-    K_inst = min(K_steps, 2000)
+    K_inst = max(200, min(K_steps, 2000))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_inst)]
     for i in range(K_inst):
         step(evs[i])
     torch.cuda.synchronize(dev)
+
+    # every kernel alone, L2 evicted before each call (the per-call bar)
+    def iso_layout():
+        if moedc.moedc_layout(idx, T, K, E, R, cap, cnt, rk, inr, sl, ws, wsb, st, stream) != 0:
+            raise RuntimeError("moedc_layout failed")
+
+    def iso_dispatch():
+        if moedc.moedc_dispatch(x, T, H, idx, sl, cnt, K, E, cap, c.dtype, recv, scales, src, st,
+                                stream) != 0:
+            raise RuntimeError("moedc_dispatch failed")
+
+    def iso_combine():
+        if moedc.moedc_combine(eo, E, cap, H, idx, sl, w, T, K, y, st, stream) != 0:
+            raise RuntimeError("moedc_combine failed")
+
+    def iso_combine_e4m3():
+        if moedc.moedc_combine_e4m3(recv, scales, 0, E, cap, H, idx, sl, w, T, K, y, st,
+                                    stream) != 0:
+            raise RuntimeError("moedc_combine_e4m3 failed")
+
+    iso_bytes = dict(nbytes, combine_e4m3=N * (H + 4 * (H // 128)) + 12 * T * K + 2 * T * H)
+    t_iso0 = time.time()
+    iso = isolated_kernels(dev, stream, {"layout": iso_layout, "dispatch": iso_dispatch,
+                                         "combine": iso_combine,
+                                         "combine_e4m3": iso_combine_e4m3}, iso_bytes)
+    torch.cuda.synchronize(dev)
+    t_iso1 = time.time()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}: {moedc.strerror(int(st.item()))}")
+    for k in ("dispatch", "combine"):
+        iso[k]["meets_70pct_of_8tbs"] = iso[k]["gbs"] >= 0.7 * HBM_NOMINAL_GBS
     time.sleep(0.3)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+    clocks_iso = sampler.summary(t_iso0, t_iso1)
 
     total_ms = start.elapsed_time(end)
     lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -680,7 +863,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "peak_source": peak_src + " (of measured)" if "measured" in
                 peak_src else peak_src, "traffic": ncu_traffic(kname),
-                "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+                "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"],
+                "achieved_from": f"mean in-step duration over {K_inst} instrumented steps",
+                "frac_isolated": {k: iso[k]["frac_of_measured_peak"]
+                                  for k in ("dispatch", "combine", "combine_e4m3")}}
 
     # ---- end to end through the public API with host buffers.  A caller that
     # streams batches overlaps the next batch's host->device copies with this
@@ -776,22 +962,16 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         c.extra["eo_host"] = eo_host
-        dt, b = oracle_step(c, c.T)
-        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "seconds": dt,
-               "sample": f"one full step of the workload (all {c.T} tokens): layout, fp8 "
-                         f"dispatch, combine; single-threaded plain-C oracle; {cpu_model()}"}
+        cpu = cpu_baseline_full(c)
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": K_steps, "warmup": W, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 dispatch / bf16 combine (fp32 arithmetic)",
             "data": "synthetic (seeded numpy: x~N(0,1) bf16, uniform distinct top-8)",
-            "config": dict(workload_config(c), parallelism=f"replicas x{world}",
-                           l2="inputs larger than L2: ~0.9 GB of HBM touched per step vs 129 MB "
-                              "L2, no flush"),
+            "config": workload_config(c, world),
             "frac_of_8tbs": value / world / HBM_NOMINAL_GBS,
-            "kernels": kern, "roofline": roofline,
+            "kernels": kern, "kernels_isolated": iso, "roofline": roofline,
             "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                     "steps": e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "path": "pinned host -> device copies of x, topk_idx, topk_weights, "
@@ -800,10 +980,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                             "moedc_dispatch, moedc_combine; y and counts back to pinned host "
                             "on a third stream"},
             "gpu_launches": launches_per_step * K_steps,
-            "kernel_timing": f"per-kernel durations from a second pass of {K_inst} steps with "
-                             "events between kernels; the step time comes from the clean pass",
+            "kernel_timing": f"kernels: in-step durations from a second pass of {K_inst} steps "
+                             "with events between kernels (the step time comes from the clean "
+                             "pass); kernels_isolated: each kernel alone, 1 GiB read before every "
+                             "call to evict L2, 20 warm-ups then "
+                             f"{iso['dispatch']['reps']} timed calls",
             "workloads": side,
-            "clocks": clocks, "cpu_baseline": cpu}
+            "clocks": clocks, "clocks_isolated": clocks_iso, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
 
 
