@@ -317,10 +317,8 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * MOEDC_SCALES_PER_TOKEN beyond 1024 entries.  Results are identical on every
  * path.
  *
- * Test hook: with the environment variable MOEDC_TEST_BARRIER_EXTRA=n set,
- * the cooperative launch's barriers wait for n blocks more than the grid has,
- * so that they run out and report MOEDC_ERR_TIMEOUT; it exists to test that
- * path and is never set in normal use.
+ * The barriers' bounded waits are tested through moedc_test_set_barrier_extra
+ * (below), never through the environment.
  */
 #define MOEDC_FUSED_MAX_ENTRIES 1024
 MOEDC_EXPORT size_t moedc_layout_dispatch_workspace_bytes(int T, int K, int E, int R);
@@ -331,6 +329,17 @@ MOEDC_EXPORT int moedc_layout_dispatch(const void* x, const int32_t* topk_idx,
                           void* recv, float* scales, int32_t* src_idx,
                           void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Test hook, not for production use.  With extra_arrivals = n > 0, every
+ * later cooperative launch of moedc_layout_dispatch makes its grid barriers
+ * wait for n blocks more than the grid has, so that each wait runs out and
+ * the call reports MOEDC_ERR_TIMEOUT on its device status; 0 (the initial
+ * value) restores normal barriers.  Process-wide and read once per call on
+ * the host (no environment lookup); it exists so that a test can drive the
+ * timeout path without a fault.
+ */
+MOEDC_EXPORT void moedc_test_set_barrier_extra(unsigned extra_arrivals);
 
 #ifdef __cplusplus
 }

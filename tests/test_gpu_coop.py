@@ -4,7 +4,6 @@ moedc_layout_dispatch_workspace_bytes):
 against the CPU oracle, against the two-launch path on the same inputs, with
 garbage in the workspace, under CUDA-graph replay, and the bounded barrier
 wait running out (a test hook makes the barrier wait for one block too many)."""
-import os
 
 import numpy as np
 import pytest
@@ -187,12 +186,13 @@ def test_coop_barrier_wait_runs_out_and_reports_timeout():
     c = case("t9000_fp8")
     d = DevCase(c)
     ws = _coop_ws(c)
-    os.environ["MOEDC_TEST_BARRIER_EXTRA"] = "1"
+    lib = moedc.load()
+    lib.moedc_test_set_barrier_extra(1)
     try:
         lay, *_ = _run(d, c, c.dtype, ws)
         torch.cuda.synchronize()
     finally:
-        del os.environ["MOEDC_TEST_BARRIER_EXTRA"]
+        lib.moedc_test_set_barrier_extra(0)
     assert int(lay.status.item()) == moedc.ERR_TIMEOUT
     lay, recv, scales, src = _run(d, c, c.dtype, ws)
     torch.cuda.synchronize()
