@@ -745,7 +745,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     wsb = moedc.moedc_layout_workspace_bytes(T, K, E, R)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-    layout_kernels = 2 if wsb > 0 else 1
+    layout_kernels = 2 if T * K > 65536 else 1     # two launches only beyond 65536 entries
     launches_per_step = layout_kernels + 2
 
     stream = torch.cuda.current_stream(dev)

@@ -1,4 +1,6 @@
-// Entry points that launch nothing: version, status text, device queries.
+// Entry points that launch nothing: version, status text, device queries,
+// the test hook of the bounded waits.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -58,7 +60,19 @@ int resident_blocks(const void* kernel, int threads, size_t smem)
     return blocks;
 }
 
+namespace {
+// moedc_test_set_wait_extra: zero unless a test sets it
+std::atomic<unsigned> g_test_wait_extra{0};
+}  // namespace
+
+unsigned test_wait_extra() { return g_test_wait_extra.load(std::memory_order_relaxed); }
+
 }  // namespace moedc_host
+
+extern "C" void moedc_test_set_wait_extra(unsigned extra_arrivals)
+{
+    moedc_host::g_test_wait_extra.store(extra_arrivals, std::memory_order_relaxed);
+}
 
 extern "C" int moedc_api_version(void) { return MOEDC_API_VERSION; }
 

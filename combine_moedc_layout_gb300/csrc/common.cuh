@@ -272,10 +272,20 @@ LayoutGeom layout_geometry(int T, int K, int E, int R);
 bool layout_args_ok(int T, int K, int E, int R, int cap);
 
 // Launches of the layout kernels (layout.cu); used by the fused entry point.
+// Up to 65536 entries a workspace of layout_onepass_workspace_bytes selects
+// the single-pass kernel (layout_onepass.cu), no workspace the sweep.
 int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
                   int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
                   uint8_t* is_token_in_rank, int32_t* slot, void* workspace,
-                  int32_t* dev_status, cudaStream_t stream);
+                  size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+size_t layout_onepass_workspace_bytes(int T, int K, int E, int R);
+// MOEDC_ERR_UNIMPLEMENTED when the shape or the workspace does not take it
+int launch_layout_onepass(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
+                          int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
+                          uint8_t* is_token_in_rank, int32_t* slot, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+// extra arrivals every bounded wait waits for (moedc_test_set_wait_extra)
+unsigned test_wait_extra();
 int launch_dispatch(const void* x, int T, int H, const int32_t* topk_idx, const int32_t* slot,
                     const int32_t* num_tokens_per_expert, int K, int E, int cap, int out_dtype,
                     void* recv, float* scales, int32_t* src_idx, int32_t* dev_status,

@@ -413,7 +413,7 @@ extern "C" int moedc_layout_dispatch(const void* x, const int32_t* topk_idx, int
             return MOEDC_ERR_ARG;
         int st = launch_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert,
                                num_tokens_per_rank, is_token_in_rank, slot, workspace,
-                               dev_status, stream);
+                               workspace_bytes, dev_status, stream);
         if (st != MOEDC_OK) return st;
         return launch_dispatch(x, T, H, topk_idx, slot, num_tokens_per_expert, K, E, cap,
                                out_dtype, recv, scales, src_idx, dev_status, stream);

@@ -375,10 +375,14 @@ static int ensure_smem_attr(const void* fn, size_t bytes)
 int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
                   int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
                   uint8_t* is_token_in_rank, int32_t* slot, void* workspace,
-                  int32_t* dev_status, cudaStream_t stream)
+                  size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream)
 {
     const LayoutGeom g = layout_geometry(T, K, E, R);
     if (g.sweep) {
+        const int st = launch_layout_onepass(topk_idx, T, K, E, R, cap, num_tokens_per_expert,
+                                             num_tokens_per_rank, is_token_in_rank, slot,
+                                             workspace, workspace_bytes, dev_status, stream);
+        if (st != MOEDC_ERR_UNIMPLEMENTED) return st;
         const bool vec_ok = aligned(topk_idx, 16);
         clear_stale_error();
         launch(moedc::layout_sweep_kernel, g.blocks, moedc::kSweepThreads, 0, stream, topk_idx, T, K, E, R, cap, vec_ok, num_tokens_per_expert, num_tokens_per_rank,
@@ -409,7 +413,9 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
 extern "C" size_t moedc_layout_workspace_bytes(int T, int K, int E, int R)
 {
     if (!moedc_host::layout_args_ok(T, K, E, R, 1)) return 0;
-    return moedc_host::layout_geometry(T, K, E, R).ws;
+    const size_t need = moedc_host::layout_geometry(T, K, E, R).ws;
+    const size_t fast = moedc_host::layout_onepass_workspace_bytes(T, K, E, R);
+    return need > fast ? need : fast;
 }
 
 extern "C" int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
@@ -428,5 +434,5 @@ extern "C" int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int R,
     if (g.ws > 0 && (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)))
         return MOEDC_ERR_ARG;
     return launch_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,
-                         is_token_in_rank, slot, workspace, dev_status, stream);
+                         is_token_in_rank, slot, workspace, workspace_bytes, dev_status, stream);
 }

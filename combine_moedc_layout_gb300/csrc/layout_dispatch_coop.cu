@@ -329,10 +329,6 @@ namespace {
 std::atomic<unsigned long long> g_epoch{
     (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull};
 
-// Test hook (moedc_test_set_barrier_extra): arrivals the barriers wait for
-// beyond the grid's own blocks.  Zero unless a test sets it.
-std::atomic<unsigned> g_test_barrier_extra{0};
-
 size_t coop_workspace_bytes(int E, int R)
 {
     return moedc::kCoopHeaderBytes + (size_t)(E + R) * moedc::kCoopMaxBlocks * sizeof(int32_t);
@@ -389,7 +385,7 @@ int launch_layout_dispatch_coop(const void* x, const int32_t* topk_idx, int T, i
     if (chunk * K > moedc::kCoopMaxEntries) return MOEDC_ERR_UNIMPLEMENTED;
 
     // test hook: extra arrivals the barriers wait for, so that they run out
-    const unsigned extra = g_test_barrier_extra.load(std::memory_order_relaxed);
+    const unsigned extra = test_wait_extra();
     const unsigned long long host_epoch = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
     auto* bar = static_cast<unsigned long long*>(workspace);
     auto* counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
@@ -432,9 +428,4 @@ extern "C" size_t moedc_layout_dispatch_workspace_bytes(int T, int K, int E, int
     const size_t a = moedc_layout_workspace_bytes(T, K, E, R);
     const size_t b = moedc_host::layout_dispatch_coop_workspace_bytes(T, K, E, R);
     return a > b ? a : b;
-}
-
-extern "C" void moedc_test_set_barrier_extra(unsigned extra_arrivals)
-{
-    moedc_host::g_test_barrier_extra.store(extra_arrivals, std::memory_order_relaxed);
 }

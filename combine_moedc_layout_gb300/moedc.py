@@ -37,7 +37,7 @@ EXPORTED = ("moedc_api_version", "moedc_strerror", "moedc_layout_workspace_bytes
             "moedc_layout", "moedc_dispatch", "moedc_combine", "moedc_layout_dispatch",
             "moedc_layout_static_scratch", "moedc_dequant_e4m3", "moedc_rank_layout",
             "moedc_rank_dispatch", "moedc_rank_combine", "moedc_combine_e4m3",
-            "moedc_layout_dispatch_workspace_bytes", "moedc_test_set_barrier_extra")
+            "moedc_layout_dispatch_workspace_bytes", "moedc_test_set_wait_extra")
 
 STATIC_SCRATCH_BYTES = 1 << 20   # MOEDC_STATIC_SCRATCH_BYTES
 
@@ -94,8 +94,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.moedc_rank_combine.restype = I
     lib.moedc_combine_e4m3.argtypes = [P, P, I, I, I, I, P, P, P, I, I, P, P, P]
     lib.moedc_combine_e4m3.restype = I
-    lib.moedc_test_set_barrier_extra.argtypes = [ctypes.c_uint]
-    lib.moedc_test_set_barrier_extra.restype = None
+    lib.moedc_test_set_wait_extra.argtypes = [ctypes.c_uint]
+    lib.moedc_test_set_wait_extra.restype = None
     if path is None:
         _lib = lib
     return lib

@@ -123,12 +123,16 @@ MOEDC_EXPORT int moedc_api_version(void);
 MOEDC_EXPORT const char* moedc_strerror(int code);
 
 /*
- * Bytes of device scratch that moedc_layout needs for this shape (0 when
- * T * K <= 65536: that layout is one launch without scratch); also enough for
+ * Bytes of device workspace for moedc_layout on this shape; also enough for
  * moedc_layout_dispatch to run as layout then dispatch.  The caller allocates
- * it (any 16-byte aligned device buffer of at least this size) and may reuse
- * it across calls that are ordered on one stream.  Returns 0 for arguments
- * that the layout would reject.
+ * it (any 16-byte aligned device buffer of at least this size, no
+ * initialisation needed) and may reuse it across calls that are ordered on
+ * one stream; calls that can run at the same time need workspaces of their
+ * own.  Up to T * K = 65536 the workspace is optional: with it the layout is
+ * a single pass over the routing table (one cooperative launch), without it
+ * (NULL) a sweep that needs no scratch, also one launch, with identical
+ * results.  Beyond 65536 it is required.  Returns 0 for arguments that the
+ * layout would reject.
  */
 MOEDC_EXPORT size_t moedc_layout_workspace_bytes(int T, int K, int E, int R);
 
@@ -142,9 +146,11 @@ MOEDC_EXPORT size_t moedc_layout_workspace_bytes(int T, int K, int E, int R);
  *   is_token_in_rank[t][r]  = 1 if any entry of token t goes to rank r.
  *   num_tokens_per_rank[r]  = number of distinct tokens with a 1 in column r.
  * Arguments: T >= 0, 1 <= K <= MOEDC_MAX_K, 1 <= E <= MOEDC_MAX_E,
- * 1 <= R <= E with E % R == 0, cap >= 1.  workspace may be NULL only when
- * moedc_layout_workspace_bytes() returns 0.
- * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE, MOEDC_ERR_CAPACITY.
+ * 1 <= R <= E with E % R == 0, cap >= 1.  workspace may be NULL (or smaller
+ * than moedc_layout_workspace_bytes()) only when T * K <= 65536.
+ * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE, MOEDC_ERR_CAPACITY, and
+ * MOEDC_ERR_TIMEOUT if a bounded wait of the single-pass layout gave up (its
+ * outputs are then unspecified; the next call starts clean).
  */
 MOEDC_EXPORT int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
                  int32_t* num_tokens_per_expert, int32_t* num_tokens_per_rank,
@@ -317,7 +323,7 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * MOEDC_SCALES_PER_TOKEN beyond 1024 entries.  Results are identical on every
  * path.
  *
- * The barriers' bounded waits are tested through moedc_test_set_barrier_extra
+ * The barriers' bounded waits are tested through moedc_test_set_wait_extra
  * (below), never through the environment.
  */
 #define MOEDC_FUSED_MAX_ENTRIES 1024
@@ -332,14 +338,16 @@ MOEDC_EXPORT int moedc_layout_dispatch(const void* x, const int32_t* topk_idx,
 
 /*
  * Test hook, not for production use.  With extra_arrivals = n > 0, every
- * later cooperative launch of moedc_layout_dispatch makes its grid barriers
- * wait for n blocks more than the grid has, so that each wait runs out and
- * the call reports MOEDC_ERR_TIMEOUT on its device status; 0 (the initial
- * value) restores normal barriers.  Process-wide and read once per call on
- * the host (no environment lookup); it exists so that a test can drive the
- * timeout path without a fault.
+ * later bounded wait of the library waits for something that never comes:
+ * the cooperative launch of moedc_layout_dispatch makes its grid barriers
+ * wait for n blocks more than the grid has, and the single-pass layout's
+ * last block also waits for the flag of a chunk that does not exist.  Each
+ * such wait runs out and the call reports MOEDC_ERR_TIMEOUT on its device
+ * status; 0 (the initial value) restores normal waits.  Process-wide, read
+ * once per call on the host (no environment lookup); it exists so that a
+ * test can drive the timeout paths without a fault.
  */
-MOEDC_EXPORT void moedc_test_set_barrier_extra(unsigned extra_arrivals);
+MOEDC_EXPORT void moedc_test_set_wait_extra(unsigned extra_arrivals);
 
 #ifdef __cplusplus
 }

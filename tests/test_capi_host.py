@@ -55,21 +55,33 @@ def test_version_and_strerror(lib):
     assert "unknown" in moedc.strerror(99)
 
 
+def _onepass_bytes(T, K, E, R):
+    """Single-pass layout workspace: a 256-byte header (the generation word),
+    then one row of E + R tagged 64-bit counts per chunk of 1024 // K tokens,
+    then two spare words."""
+    chunks = max(1, -(-T // (1024 // K)))
+    return 256 + (chunks * (E + R) + 2) * 8
+
+
 def test_workspace_bytes(lib):
-    # up to 65536 entries the layout is a single launch without scratch
-    assert moedc.moedc_layout_workspace_bytes(64, 4, 32, 4) == 0
-    assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == 0
-    assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 0
-    assert moedc.moedc_layout_workspace_bytes(8192, 8, 256, 8) == 0
+    # up to 65536 entries: the single-pass layout's workspace (optional there)
+    assert moedc.moedc_layout_workspace_bytes(64, 4, 32, 4) == _onepass_bytes(64, 4, 32, 4) == 560
+    assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == _onepass_bytes(128, 8, 288, 8)
+    assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 256 + (32 * 264 + 2) * 8
+    assert moedc.moedc_layout_workspace_bytes(8192, 8, 256, 8) == _onepass_bytes(8192, 8, 256, 8)
+    assert moedc.moedc_layout_workspace_bytes(0, 8, 256, 8) == _onepass_bytes(0, 8, 256, 8)
+    assert moedc.moedc_layout_workspace_bytes(2048, 32, 1024, 1024) == \
+        _onepass_bytes(2048, 32, 1024, 1024)
     # beyond: 128 tokens per block -> blocks x (E + R) int32
     assert moedc.moedc_layout_workspace_bytes(8193, 8, 256, 8) == 65 * (256 + 8) * 4
     assert moedc.moedc_layout_workspace_bytes(40000, 8, 128, 8) == 313 * (128 + 8) * 4
-    # the one-call layout+dispatch: none while the layout is one sweep launch
-    # (fused block, or layout then dispatch), beyond it the cooperative
-    # launch's barrier words and count rows [E + R][2048]
-    assert moedc.moedc_layout_dispatch_workspace_bytes(128, 8, 288, 8) == 0
-    assert moedc.moedc_layout_dispatch_workspace_bytes(4096, 8, 256, 8) == 0
-    assert moedc.moedc_layout_dispatch_workspace_bytes(8192, 8, 256, 8) == 0
+    # the one-call layout+dispatch: the layout's workspace while the layout
+    # is one launch (fused block, or layout then dispatch), beyond it the
+    # cooperative launch's barrier words and count rows [E + R][2048]
+    assert moedc.moedc_layout_dispatch_workspace_bytes(128, 8, 288, 8) == \
+        _onepass_bytes(128, 8, 288, 8)
+    assert moedc.moedc_layout_dispatch_workspace_bytes(4096, 8, 256, 8) == \
+        _onepass_bytes(4096, 8, 256, 8)
     assert moedc.moedc_layout_dispatch_workspace_bytes(8193, 8, 256, 8) == 256 + 264 * 2048 * 4
     assert moedc.moedc_layout_dispatch_workspace_bytes(40000, 8, 128, 8) == 256 + 136 * 2048 * 4
     assert moedc.moedc_layout_dispatch_workspace_bytes(4096, 8, 250, 8) == 0

@@ -187,12 +187,12 @@ def test_coop_barrier_wait_runs_out_and_reports_timeout():
     d = DevCase(c)
     ws = _coop_ws(c)
     lib = moedc.load()
-    lib.moedc_test_set_barrier_extra(1)
+    lib.moedc_test_set_wait_extra(1)
     try:
         lay, *_ = _run(d, c, c.dtype, ws)
         torch.cuda.synchronize()
     finally:
-        lib.moedc_test_set_barrier_extra(0)
+        lib.moedc_test_set_wait_extra(0)
     assert int(lay.status.item()) == moedc.ERR_TIMEOUT
     lay, recv, scales, src = _run(d, c, c.dtype, ws)
     torch.cuda.synchronize()

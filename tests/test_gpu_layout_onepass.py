@@ -1,0 +1,169 @@
+"""GPU parity of the two one-launch layouts for up to 65536 routing entries:
+the single-pass layout (with a workspace) and the sweep (without one), each
+against the CPU oracle bit for bit, plus the single-pass layout's workspace
+rules: any initial contents, reuse across shapes, replays of a captured graph
+with new routing, and a bounded wait that runs out (MOEDC_ERR_TIMEOUT, after
+which the next call is correct)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moedc_layout_gb300 import moedc, synth
+from parity_util import DevCase, compare_layout
+
+pytestmark = pytest.mark.gpu
+
+NAMED = ["tiny", "low4", "low16", "default_ll", "throughput", "imbalanced"]
+RANDOM = {
+    "multichunk_k6": dict(seed=31, T=3001, H=8, K=6, E=96, R=12, cap=None, dtype=synth.BF16,
+                          mask_p=0.07),
+    "k1": dict(seed=32, T=9000, H=8, K=1, E=16, R=4, cap=None, dtype=synth.BF16),
+    "k32_e1024": dict(seed=33, T=2048, H=8, K=32, E=1024, R=8, cap=None, dtype=synth.BF16),
+    "e_eq_r_1024": dict(seed=34, T=600, H=8, K=8, E=1024, R=1024, cap=None, dtype=synth.BF16,
+                        mask_p=0.02),
+    "one_expert": dict(seed=35, T=5000, H=8, K=1, E=1, R=1, cap=None, dtype=synth.BF16),
+    "duplicates": dict(seed=36, T=900, H=8, K=8, E=5, R=5, cap=None, dtype=synth.BF16,
+                       distinct=False),
+    "t1": dict(seed=37, T=1, H=8, K=8, E=256, R=8, cap=1, dtype=synth.BF16),
+    "max_entries": dict(seed=38, T=8192, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16,
+                        mask_p=0.1),
+    "chunk_edge": dict(seed=39, T=129, H=8, K=8, E=64, R=8, cap=None, dtype=synth.BF16),
+    "k3_ragged": dict(seed=40, T=21845, H=8, K=3, E=48, R=6, cap=None, dtype=synth.BF16,
+                      mask_p=0.3),
+}
+
+
+def _case(key):
+    return synth.make_case(key) if key in NAMED else synth.make_random_case(**RANDOM[key])
+
+
+def _outputs(T, K, E, R):
+    dev = "cuda"
+    return dict(cnt=torch.full((E,), -7, dtype=torch.int32, device=dev),
+                rk=torch.full((R,), -7, dtype=torch.int32, device=dev),
+                inr=torch.full((T, R), 9, dtype=torch.uint8, device=dev),
+                slot=torch.full((T, K), -7, dtype=torch.int32, device=dev),
+                st=torch.zeros(1, dtype=torch.int32, device=dev))
+
+
+class _Lay:
+    def __init__(self, o):
+        self.num_tokens_per_expert = o["cnt"]
+        self.num_tokens_per_rank = o["rk"]
+        self.is_token_in_rank = o["inr"]
+        self.slot = o["slot"]
+        self.status = o["st"]
+
+
+def _run(idx, c, ws, stream=None):
+    o = _outputs(c.T, c.K, c.E, c.R)
+    wsb = 0 if ws is None else ws.numel()
+    rc = moedc.moedc_layout(idx, c.T, c.K, c.E, c.R, c.cap, o["cnt"], o["rk"], o["inr"],
+                            o["slot"], ws, wsb, o["st"], stream)
+    assert rc == moedc.OK
+    return o
+
+
+def _check(o, c):
+    torch.cuda.synchronize()
+    ref = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    compare_layout(_Lay(o), ref, c.T)
+    assert int(o["st"].item()) == ref["status"]
+
+
+@pytest.mark.parametrize("key", NAMED + list(RANDOM))
+@pytest.mark.parametrize("path", ["onepass", "sweep"])
+def test_layout_paths_match_oracle(key, path):
+    c = _case(key)
+    assert c.T * c.K <= 65536
+    d = DevCase(c)
+    ws = None
+    if path == "onepass":
+        n = moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R)
+        assert n > 0
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    _check(_run(d.topk_idx, c, ws), c)
+
+
+@pytest.mark.parametrize("fill", ["zeros", "ones", "random"])
+def test_onepass_any_workspace_contents(fill):
+    c = _case("throughput")
+    d = DevCase(c)
+    n = moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R)
+    if fill == "zeros":
+        ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    elif fill == "ones":
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+    else:
+        g = torch.Generator(device="cuda").manual_seed(5)
+        ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+    _check(_run(d.topk_idx, c, ws), c)
+
+
+def test_onepass_workspace_reused_across_shapes_and_routings():
+    # one workspace, large enough for the largest shape, calls back to back
+    keys = ["max_entries", "tiny", "throughput", "k32_e1024", "t1", "multichunk_k6", "throughput"]
+    cases = [_case(k) for k in keys]
+    n = max(moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R) for c in cases)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    outs = []
+    for c in cases:
+        outs.append((c, _run(DevCase(c).topk_idx, c, ws)))
+    for c, o in outs:
+        _check(o, c)
+
+
+def test_onepass_graph_replays_with_new_routing():
+    """Replays of one captured call share the host epoch; the workspace's
+    generation must still keep one replay's flags from releasing the next."""
+    base = _case("throughput")
+    T, K, E, R = base.T, base.K, base.E, base.R
+    idx = torch.from_numpy(base.topk_idx).cuda()
+    n = moedc.moedc_layout_workspace_bytes(T, K, E, R)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    o = _outputs(T, K, E, R)
+
+    def call(stream):
+        assert moedc.moedc_layout(idx, T, K, E, R, base.cap, o["cnt"], o["rk"], o["inr"],
+                                  o["slot"], ws, n, o["st"], stream) == moedc.OK
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(s)                                   # warm-up outside the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call(s)
+    torch.cuda.synchronize()
+    for seed in (50, 51, 52):
+        c = synth.make_random_case(seed, T=T, H=8, K=K, E=E, R=R, cap=None, dtype=synth.BF16,
+                                   mask_p=0.05)
+        c.cap = base.cap            # the captured call's cap
+        idx.copy_(torch.from_numpy(c.topk_idx))
+        o["st"].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.layout(c.topk_idx, E, R, base.cap)
+        compare_layout(_Lay(o), ref, T)
+        assert int(o["st"].item()) == ref["status"]
+
+
+@pytest.mark.parametrize("key", ["throughput", "tiny"])
+def test_onepass_wait_runs_out_and_reports_timeout(key):
+    """A bounded wait of the single-pass layout that runs out raises
+    MOEDC_ERR_TIMEOUT (the test hook makes the last block wait for a flag no
+    block writes), the context stays usable and the next call is correct."""
+    c = _case(key)
+    d = DevCase(c)
+    n = moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    lib = moedc.load()
+    lib.moedc_test_set_wait_extra(1)
+    try:
+        o = _run(d.topk_idx, c, ws)
+        torch.cuda.synchronize()
+    finally:
+        lib.moedc_test_set_wait_extra(0)
+    assert int(o["st"].item()) == moedc.ERR_TIMEOUT
+    _check(_run(d.topk_idx, c, ws), c)
