@@ -31,14 +31,14 @@
 // end.  A wait that runs out raises MOEDC_ERR_TIMEOUT.
 //
 // Epochs: a launch's epoch is the per-call host counter plus a generation
-// word of the workspace times an odd constant, cut to 53 bits (a count takes
-// the low 11: a chunk never counts past 1024).  Every block reads the
+// word of the workspace times an odd constant, cut to 51 bits (a count takes
+// the low 13: a chunk never counts past 4096).  Every block reads the
 // generation at its start; the last block advances it only after it has
 // read every other block's row (so every block has read the generation),
 // and a block that gives up advances it too.  Words left by earlier
 // launches, by earlier replays of one captured graph (same host counter) or
 // by uninitialised memory therefore do not carry the epoch (a random word
-// matches with probability 2^-53): the workspace needs no initialisation.
+// matches with probability 2^-51): the workspace needs no initialisation.
 #include <atomic>
 #include <chrono>
 #include <climits>
@@ -49,10 +49,16 @@ namespace moedc {
 
 constexpr int kOpThreads = 1024;
 constexpr int kOpWarps = kOpThreads / kWarp;
-constexpr int kOpMaxEntries = kOpThreads;      // routing entries of one chunk
+// routing entries per thread: a chunk holds 1024 * kOpEntriesPerThread
+// entries, a warp kOpEntriesPerThread consecutive 32-entry tiles
+#ifndef MOEDC_OP_EPT
+#define MOEDC_OP_EPT 1
+#endif
+constexpr int kOpEntriesPerThread = MOEDC_OP_EPT;
+constexpr int kOpMaxEntries = kOpThreads * kOpEntriesPerThread;   // of one chunk
 constexpr int kOpMaxChunks = 128;
 constexpr size_t kOpHeaderBytes = 256;         // generation word, then padding
-constexpr int kOpCountBits = 11;               // a chunk's counts are <= 1024
+constexpr int kOpCountBits = 13;               // a chunk's counts are <= 4096
 constexpr unsigned long long kOpCountMask = (1ull << kOpCountBits) - 1;
 constexpr unsigned long long kOpTagMask = (1ull << (64 - kOpCountBits)) - 1;
 constexpr long long kOpSpinLimit = 1ll << 21;   // polls, 64 ns sleeps after the first 64: >= 0.13 s
@@ -99,6 +105,9 @@ __device__ int op_count_when_tagged(const unsigned long long* p, unsigned long l
 //   s_pre [E + R]            entries / tokens of the chunks before this one
 //   s_ids [kOpMaxEntries]    the chunk's expert ids; later the partial sums
 //                            of step 4
+// Warp w owns the chunk's entries [w * 32 * EPT, (w + 1) * 32 * EPT), EPT
+// tiles of 32 in order; thread (w, lane) holds entry w * 32 * EPT + 32 u +
+// lane of tile u.
 __global__ void __launch_bounds__(kOpThreads, 1)
 layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, int R,
                       int cap, int tpc, int32_t* __restrict__ num_tokens_per_expert,
@@ -129,25 +138,45 @@ layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E,
     const int epr = E / R;
 
     // 1. the chunk's ids (in flight while shared memory is cleared) and the epoch
-    int e = -1;
-    if (tid < n) e = __ldg(topk_idx + (int64_t)t0 * K + tid);
+    constexpr int EPT = kOpEntriesPerThread;
+    const int i0 = warp * kWarp * EPT + lane;   // entry of tile 0; tile u adds 32 u
+    int e[EPT];
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) {
+        const int i = i0 + u * kWarp;
+        e[u] = i < n ? __ldg(topk_idx + (int64_t)t0 * K + i) : -1;
+    }
     if (tid == 0) {
         const unsigned long long gen = __ldcg(ws_generation);
         s_tag = ((host_epoch + gen * kOpEpochStride) | 1ull) & kOpTagMask;
     }
     for (int i = tid; i < kOpWarps * wstride; i += kOpThreads) s_wc[i] = 0;
     for (int i = tid; i < R; i += kOpThreads) s_cnt[E + i] = 0;
-    if (tid < n) s_ids[tid] = e;
+#pragma unroll
+    for (int u = 0; u < EPT; ++u)
+        if (i0 + u * kWarp < n) s_ids[i0 + u * kWarp] = e[u];
     __syncthreads();
     const unsigned long long tag = s_tag;
 
-    // 2. in-chunk ranks and counts
-    const bool valid = tid < n && e >= 0 && e < E;
-    const bool bad = tid < n && e != -1 && !valid;
-    const unsigned peers = match_expert(e, valid);
-    const unsigned before = peers & lanemask_lt();
-    const int tile_rank = __popc(before);
-    if (valid && before == 0) s_wc[warp * wstride + e] = __popc(peers);
+    // 2. in-chunk ranks and counts: tile by tile, an entry's rank in its warp
+    //    is the warp's running count of its expert plus its rank in the tile
+    bool bad = false;
+    unsigned valid_bits = 0;
+    int rank[EPT];
+    int32_t* my_wc = s_wc + warp * wstride;
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) {
+        const bool in_chunk = i0 + u * kWarp < n;
+        const bool valid = in_chunk && e[u] >= 0 && e[u] < E;
+        bad = bad || (in_chunk && e[u] != -1 && !valid);
+        valid_bits |= (valid ? 1u : 0u) << u;
+        const unsigned peers = match_expert(e[u], valid);
+        const unsigned before = peers & lanemask_lt();
+        rank[u] = valid ? my_wc[e[u]] + __popc(before) : 0;
+        __syncwarp();
+        if (valid && before == 0) my_wc[e[u]] += __popc(peers);
+        __syncwarp();
+    }
     // token-in-rank rows of this chunk, and per rank its tokens that reach it.
     // When R divides the block, every pair a thread visits has rank tid % R:
     // the thread sums its own pairs and lanes of equal rank combine by
@@ -226,21 +255,38 @@ layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E,
         const int c = G > 1 ? tid - g * ER : c0 + tid;
         int acc = 0;
         if (g < G && c < ER) {
-            for (int j0 = g; j0 < b; j0 += G * kOpBatch) {
+            for (int j0 = g; j0 < b && ok; j0 += G * kOpBatch) {
+                // a batch of words, re-polled together until each carries the
+                // epoch: the loads of one round are all in flight at once
                 unsigned long long w[kOpBatch];
+                unsigned pending = 0;
 #pragma unroll
                 for (int u = 0; u < kOpBatch; ++u) {
                     const int j = j0 + u * G;
-                    w[u] = j < b ? op_ld_relaxed(ws_rows + (int64_t)j * ER + c) : 0;
-                }
-#pragma unroll
-                for (int u = 0; u < kOpBatch; ++u) {
-                    const int j = j0 + u * G;
+                    w[u] = 0;
                     if (j < b) {
-                        const int v = op_count_when_tagged(ws_rows + (int64_t)j * ER + c, w[u], tag);
-                        if (v < 0) ok = false;
-                        acc += v;
+                        w[u] = op_ld_relaxed(ws_rows + (int64_t)j * ER + c);
+                        pending |= 1u << u;
                     }
+                }
+                for (long long it = 0;; ++it) {
+#pragma unroll
+                    for (int u = 0; u < kOpBatch; ++u) {
+                        if (((pending >> u) & 1u) && (w[u] >> kOpCountBits) == tag) {
+                            acc += (int)(w[u] & kOpCountMask);
+                            pending &= ~(1u << u);
+                        }
+                    }
+                    if (pending == 0) break;
+                    if (it >= kOpSpinLimit) {
+                        ok = false;
+                        break;
+                    }
+                    if (it >= 64) __nanosleep(64);   // spin first: rows are microseconds away
+#pragma unroll
+                    for (int u = 0; u < kOpBatch; ++u)
+                        if ((pending >> u) & 1u)
+                            w[u] = op_ld_relaxed(ws_rows + (int64_t)(j0 + u * G) * ER + c);
                 }
             }
         }
@@ -272,9 +318,13 @@ layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E,
     }
 
     // 5. slots; totals from the last chunk
-    if (tid < n)
-        __stcs(slot + (int64_t)t0 * K + tid,
-               valid ? s_pre[e] + s_wc[warp * wstride + e] + tile_rank : -1);
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) {
+        const int i = i0 + u * kWarp;
+        if (i < n)
+            __stcs(slot + (int64_t)t0 * K + i,
+                   ((valid_bits >> u) & 1u) ? s_pre[e[u]] + my_wc[e[u]] + rank[u] : -1);
+    }
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);
     if (b == nb - 1) {
         for (int c = tid; c < ER; c += kOpThreads) {
