@@ -80,15 +80,16 @@ __device__ __forceinline__ SliceX load_slice_fp8(const uint16_t* __restrict__ xr
 
 // kScaleCols: scales stored [E][G][cap] (group-major per expert) instead of
 // [E][cap][G]; lane k then also holds my_sbase = e * G * cap + s for entry k.
-template <bool kScaleCols>
-__device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slice, int lane,
-                                                int K, int my_row, int64_t my_sbase, int cap,
-                                                uint8_t* __restrict__ recv,
-                                                float* __restrict__ scales)
+// The lane's 16 codes and its group's scale: amax over the 8 lanes of the
+// group (three xor shuffles), clamped, one division for the scale and one per
+// element for the codes.
+struct SliceQ {
+    uint4 q;
+    float sc;
+};
+
+__device__ __forceinline__ SliceQ quant_slice_fp8(const SliceX& v)
 {
-    const int G = H / 128;
-    const int c0 = slice * kSlice + lane * 16;
-    const bool act = c0 < H;
     const uint32_t w[8] = {v.a.x, v.a.y, v.a.z, v.a.w, v.b.x, v.b.y, v.b.z, v.b.w};
     float f[16];
 #pragma unroll
@@ -112,7 +113,21 @@ __device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slic
         const uint32_t hi = quant_pair(f[4 * j + 2], f[4 * j + 3], sc);
         p[j] = lo | (hi << 16);
     }
-    const uint4 q = make_uint4(p[0], p[1], p[2], p[3]);
+    return SliceQ{make_uint4(p[0], p[1], p[2], p[3]), sc};
+}
+
+template <bool kScaleCols>
+__device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slice, int lane,
+                                                int K, int my_row, int64_t my_sbase, int cap,
+                                                uint8_t* __restrict__ recv,
+                                                float* __restrict__ scales)
+{
+    const int G = H / 128;
+    const int c0 = slice * kSlice + lane * 16;
+    const bool act = c0 < H;
+    const SliceQ sq = quant_slice_fp8(v);
+    const uint4 q = sq.q;
+    const float sc = sq.sc;
     const bool leader = (lane & 7) == 0;
     const int g = c0 / 128;
     for (int k = 0; k < K; ++k) {
