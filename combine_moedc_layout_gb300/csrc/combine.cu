@@ -250,13 +250,15 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
 }
 
 // K <= 8: a warp owns half of a token's 512-channel slices; the routing of
-// its rows (row offset, weight, scale base) is derived once and kept in
-// registers across those slices.  Each row's shuffles, 64-bit address
-// arithmetic and scale-index work were otherwise redone for every slice; with
-// 4.5 instructions per element per term the kernel is bound by issue, and
-// hoisting them took the 4096-token workload from 75.8 to 59.4 us.
+// its rows (row index, weight, scale base) is derived once and kept in
+// registers across those slices.  Each row's shuffles, address arithmetic
+// and scale-index work were otherwise redone for every slice; hoisting them
+// took the 4096-token workload from 75.8 to 59.4 us, packed binary32
+// multiplies to 55.3 us, and 32-bit row indices with three blocks per SM
+// (at two, ncu showed 24% of warps active and load waits as the first stall)
+// to 53.5-54.0 us.
 constexpr int kHalves = 2;   // measured: 1 part 63.5 us, 2 parts 59.4, 3 parts 60.4, 4 parts 68.6
-__global__ void __launch_bounds__(kCombineThreads, 2)
+__global__ void __launch_bounds__(kCombineThreads, 3)
 combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __restrict__ scales,
                          int scale_mode, int E, int cap, int H,
                          const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
@@ -283,9 +285,11 @@ combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __
             my_w = __ldg(topk_weights + (int64_t)t * K + lane);
             if (half == 0 && (my_e < -1 || my_e >= E)) bad = true;
         }
-        int64_t roff[kCombine8Batch];
-        int64_t sbase[kCombine8Batch];
-        int64_t sstep;   // scale index step per 128-channel group
+        // 32-bit row indices and scale bases (the host bounds E * cap * H / 128 by
+        // INT32_MAX): fewer registers
+        int rowi[kCombine8Batch];
+        int sbase[kCombine8Batch];
+        int sstep;   // scale index step per 128-channel group
         float wk[kCombine8Batch];
         unsigned okm = 0;
 #pragma unroll
@@ -295,10 +299,10 @@ combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __
             wk[j] = __shfl_sync(0xffffffffu, my_w, j);
             const bool ok = j < K && e >= 0 && e < E && sidx >= 0 && sidx < cap;
             okm |= (ok ? 1u : 0u) << j;
-            const int64_t row = ok ? (int64_t)e * cap + sidx : 0;
-            roff[j] = row * H;
+            const int row = ok ? e * cap + sidx : 0;
+            rowi[j] = row;
             sbase[j] = !ok ? 0 : scale_mode == 2 ? row
-                         : scale_mode == 1 ? (int64_t)e * G * cap + sidx : row * G;
+                         : scale_mode == 1 ? e * G * cap + sidx : row * G;
         }
         sstep = scale_mode == 2 ? 0 : scale_mode == 1 ? cap : 1;
         const int sl_end = min(nslice, (half + 1) * per_half);
@@ -310,8 +314,8 @@ combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __
             float sc[kCombine8Batch];
 #pragma unroll
             for (int j = 0; j < kCombine8Batch; ++j) {
-                q[j] = ld_global_nc(reinterpret_cast<const uint4*>(expert_out + roff[j] +
-                                                                    (act ? c0 : 0)));
+                q[j] = ld_global_nc(reinterpret_cast<const uint4*>(
+                    expert_out + (int64_t)rowi[j] * H + (act ? c0 : 0)));
                 sc[j] = __ldg(scales + (((okm >> j) & 1u) ? sbase[j] + g * sstep : 0));
             }
             float2 acc[8];   // channel pairs
