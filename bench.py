@@ -766,6 +766,21 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         if r != 0:
             raise RuntimeError(f"libmoedc returned {r}")
 
+    if args.profile_steps:
+        # a short run for profiler captures: the step's three kernels, then the
+        # e4m3 combine over the dispatched rows, profile_steps times
+        for _ in range(args.profile_steps):
+            step()
+            if moedc.moedc_combine_e4m3(recv, scales, 0, E, cap, H, idx, sl, w, T, K, y, st,
+                                        stream) != 0:
+                raise RuntimeError("moedc_combine_e4m3 failed")
+        torch.cuda.synchronize(dev)
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        if rank == 0:
+            print(json.dumps({"profile_steps": args.profile_steps, "workload": workload_config(c)}))
+        return
+
     K_steps, W = args.steps, max(3, args.warmup)
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -999,6 +1014,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the low-token / 128-token / imbalanced side measurements")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="only run this many steps (layout, e4m3 dispatch, combine, then the "
+                         "e4m3 combine) and exit: a short command for profiler captures")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
