@@ -21,6 +21,9 @@
 //  * Every call in the process shares the one array.  Calls whose kernels
 //    overlap on the GPU (different streams, or different host threads without
 //    ordering) race on it and give wrong slots; order them on one stream.
+//  * The cached address is that of the device's primary context at the first
+//    call.  cudaDeviceReset recreates the context and the array with it, so a
+//    process must not reset a device after using this entry point on it.
 //  * Nothing in the array needs to start at zero: the first layout kernel
 //    writes every word the second one reads, so the leftovers of an earlier
 //    call do no harm.

@@ -172,7 +172,11 @@ MOEDC_EXPORT int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int 
  *  - the first call on a device looks up the array's device address and
  *    caches it; make that first call before any stream capture begins;
  *  - all calls share the array, so calls that overlap on the GPU race and
- *    give wrong results: order them on one stream.
+ *    give wrong results: order them on one stream;
+ *  - the cached address belongs to the device's current primary context: do
+ *    not call cudaDeviceReset on a device after this entry point has run on
+ *    it (the array is recreated at a new address and later calls would write
+ *    through the stale one).
  * The call allocates nothing and calls no allocating routine.
  */
 #define MOEDC_STATIC_SCRATCH_BYTES (1u << 20)

@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_moedc_layout_gb300 import moedc, synth
 
 pytestmark = pytest.mark.gpu
@@ -103,3 +104,53 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     torch.cuda.synchronize()
     assert (o["cnt"].cpu().numpy() == -7).all()      # nothing was launched
     assert int(o["st"].item()) == 0
+
+
+def _same_as_oracle(got, c):
+    ref = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    np.testing.assert_array_equal(got["cnt"].cpu().numpy(), ref["num_tokens_per_expert"])
+    np.testing.assert_array_equal(got["rk"].cpu().numpy(), ref["num_tokens_per_rank"])
+    np.testing.assert_array_equal(got["inr"].cpu().numpy(), ref["is_token_in_rank"])
+    np.testing.assert_array_equal(got["slot"].cpu().numpy(), ref["slot"])
+    assert int(got["st"].item()) == ref["status"]
+
+
+@pytest.mark.parametrize("shape", [
+    # two kernels with scratch (beyond 65536 entries)
+    dict(seed=44, T=12000, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16, mask_p=0.05),
+    # the single-pass layout, its scratch in the static array too (4096 tokens)
+    dict(seed=45, T=4096, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16),
+])
+def test_static_scratch_matches_oracle_directly(shape):
+    c = synth.make_random_case(**shape)
+    idx = torch.from_numpy(c.topk_idx).cuda()
+    for _ in range(2):                      # twice in a row on the shared array
+        got = _static(idx, c.T, c.K, c.E, c.R, c.cap)
+        torch.cuda.synchronize()
+        _same_as_oracle(got, c)
+
+
+def test_static_scratch_call_allocates_nothing():
+    """After a first call on the device (which looks up the array's address),
+    further calls change neither torch's allocator nor the device's free
+    memory: the scratch is the array inside the library."""
+    c = synth.make_random_case(46, T=12000, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16)
+    idx = torch.from_numpy(c.topk_idx).cuda()
+    o = _outputs(c.T, c.K, c.E, c.R)
+
+    def call():
+        assert moedc.moedc_layout_static_scratch(idx, c.T, c.K, c.E, c.R, c.cap, o["cnt"],
+                                                 o["rk"], o["inr"], o["slot"],
+                                                 o["st"]) == moedc.OK
+
+    call()
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    _same_as_oracle(o, c)
