@@ -1,5 +1,5 @@
-// Routing layout in one pass over the routing table (up to 65536 entries,
-// with a caller workspace).
+// Routing layout in one pass over the routing table (from 4 chunks of 1024
+// entries up to 65536 entries, with a caller workspace).
 //
 // Sources: UCCL PR #749 "[EP] Low-latency mode batch tokens per destination"
 // (code excerpt: per-expert routed-token counters published for the ranks
@@ -57,6 +57,10 @@ constexpr int kOpWarps = kOpThreads / kWarp;
 constexpr int kOpEntriesPerThread = MOEDC_OP_EPT;
 constexpr int kOpMaxEntries = kOpThreads * kOpEntriesPerThread;   // of one chunk
 constexpr int kOpMaxChunks = 128;
+// Fewer chunks than this take the sweep: one or two blocks rank everything
+// serially, while the sweep spreads it over E + R blocks (measured at 1024
+// entries: 9.8 us single pass, 8.2 us sweep).
+constexpr int kOpMinChunks = 4;
 constexpr size_t kOpHeaderBytes = 256;         // generation word, then padding
 constexpr int kOpCountBits = 13;               // a chunk's counts are <= 4096
 constexpr unsigned long long kOpCountMask = (1ull << kOpCountBits) - 1;
@@ -372,7 +376,7 @@ size_t layout_onepass_workspace_bytes(int T, int K, int E, int R)
     if ((int64_t)T * K > 65536 || T < 0 || K < 1) return 0;
     const int tpc = op_tokens_per_chunk(K);
     const int64_t chunks = T > 0 ? ((int64_t)T + tpc - 1) / tpc : 1;
-    if (chunks > moedc::kOpMaxChunks) return 0;
+    if (chunks > moedc::kOpMaxChunks || chunks < moedc::kOpMinChunks) return 0;
     return moedc::kOpHeaderBytes + ((size_t)chunks * (E + R) + 2) * sizeof(unsigned long long);
 }
 

@@ -128,9 +128,10 @@ MOEDC_EXPORT const char* moedc_strerror(int code);
  * it (any 16-byte aligned device buffer of at least this size, no
  * initialisation needed) and may reuse it across calls that are ordered on
  * one stream; calls that can run at the same time need workspaces of their
- * own.  Up to T * K = 65536 the workspace is optional: with it the layout is
- * a single pass over the routing table (one cooperative launch), without it
- * (NULL) a sweep that needs no scratch, also one launch, with identical
+ * own.  Up to T * K = 3072 the layout is one sweep launch that needs no
+ * workspace (the query returns 0).  From 3073 to 65536 entries the workspace
+ * is optional: with it the layout is a single pass over the routing table
+ * (one cooperative launch), without it (NULL) the sweep, with identical
  * results.  Beyond 65536 it is required.  Returns 0 for arguments that the
  * layout would reject.
  */

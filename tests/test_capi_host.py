@@ -58,18 +58,21 @@ def test_version_and_strerror(lib):
 def _onepass_bytes(T, K, E, R):
     """Single-pass layout workspace: a 256-byte header (the generation word),
     then one row of E + R tagged 64-bit counts per chunk of 1024 // K tokens,
-    then two spare words."""
+    then two spare words; 0 below 4 chunks, where the sweep runs."""
     chunks = max(1, -(-T // (1024 // K)))
-    return 256 + (chunks * (E + R) + 2) * 8
+    return 256 + (chunks * (E + R) + 2) * 8 if chunks >= 4 else 0
 
 
 def test_workspace_bytes(lib):
-    # up to 65536 entries: the single-pass layout's workspace (optional there)
-    assert moedc.moedc_layout_workspace_bytes(64, 4, 32, 4) == _onepass_bytes(64, 4, 32, 4) == 560
-    assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == _onepass_bytes(128, 8, 288, 8)
+    # up to 3072 entries (fewer than 4 chunks): the sweep, no workspace
+    assert moedc.moedc_layout_workspace_bytes(64, 4, 32, 4) == 0
+    assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == 0
+    assert moedc.moedc_layout_workspace_bytes(384, 8, 256, 8) == 0
+    assert moedc.moedc_layout_workspace_bytes(0, 8, 256, 8) == 0
+    # from 4 chunks to 65536 entries: the single-pass layout's (optional) workspace
+    assert moedc.moedc_layout_workspace_bytes(512, 8, 256, 8) == _onepass_bytes(512, 8, 256, 8) > 0
     assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 256 + (32 * 264 + 2) * 8
     assert moedc.moedc_layout_workspace_bytes(8192, 8, 256, 8) == _onepass_bytes(8192, 8, 256, 8)
-    assert moedc.moedc_layout_workspace_bytes(0, 8, 256, 8) == _onepass_bytes(0, 8, 256, 8)
     assert moedc.moedc_layout_workspace_bytes(2048, 32, 1024, 1024) == \
         _onepass_bytes(2048, 32, 1024, 1024)
     # beyond: 128 tokens per block -> blocks x (E + R) int32
@@ -78,8 +81,7 @@ def test_workspace_bytes(lib):
     # the one-call layout+dispatch: the layout's workspace while the layout
     # is one launch (fused block, or layout then dispatch), beyond it the
     # cooperative launch's barrier words and count rows [E + R][2048]
-    assert moedc.moedc_layout_dispatch_workspace_bytes(128, 8, 288, 8) == \
-        _onepass_bytes(128, 8, 288, 8)
+    assert moedc.moedc_layout_dispatch_workspace_bytes(128, 8, 288, 8) == 0
     assert moedc.moedc_layout_dispatch_workspace_bytes(4096, 8, 256, 8) == \
         _onepass_bytes(4096, 8, 256, 8)
     assert moedc.moedc_layout_dispatch_workspace_bytes(8193, 8, 256, 8) == 256 + 264 * 2048 * 4

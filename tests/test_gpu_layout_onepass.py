@@ -29,6 +29,10 @@ RANDOM = {
     "max_entries": dict(seed=38, T=8192, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16,
                         mask_p=0.1),
     "chunk_edge": dict(seed=39, T=129, H=8, K=8, E=64, R=8, cap=None, dtype=synth.BF16),
+    "four_chunks": dict(seed=41, T=512, H=8, K=8, E=64, R=8, cap=None, dtype=synth.BF16,
+                        mask_p=0.05),
+    "four_chunks_ragged": dict(seed=42, T=450, H=8, K=8, E=24, R=3, cap=None,
+                               dtype=synth.BF16),
     "k3_ragged": dict(seed=40, T=21845, H=8, K=3, E=48, R=6, cap=None, dtype=synth.BF16,
                       mask_p=0.3),
 }
@@ -36,6 +40,15 @@ RANDOM = {
 
 def _case(key):
     return synth.make_case(key) if key in NAMED else synth.make_random_case(**RANDOM[key])
+
+
+def _chunks(c):
+    return max(1, -(-c.T // (1024 // c.K)))
+
+
+# the single-pass layout runs from 4 chunks of 1024 entries; below, the sweep
+SMALL = ["tiny", "low4", "low16", "default_ll", "t1", "chunk_edge"]
+ONEPASS = [k for k in NAMED + list(RANDOM) if k not in SMALL]
 
 
 def _outputs(T, K, E, R):
@@ -72,17 +85,29 @@ def _check(o, c):
     assert int(o["st"].item()) == ref["status"]
 
 
-@pytest.mark.parametrize("key", NAMED + list(RANDOM))
-@pytest.mark.parametrize("path", ["onepass", "sweep"])
-def test_layout_paths_match_oracle(key, path):
+@pytest.mark.parametrize("key", [pytest.param(k, id="onepass-" + k) for k in ONEPASS] +
+                         [pytest.param(k, id="sweep-" + k) for k in NAMED + list(RANDOM)])
+def test_layout_paths_match_oracle(request, key):
     c = _case(key)
     assert c.T * c.K <= 65536
     d = DevCase(c)
     ws = None
-    if path == "onepass":
+    if request.node.callspec.id.startswith("onepass"):
         n = moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R)
-        assert n > 0
+        assert _chunks(c) >= 4 and n > 0
         ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    _check(_run(d.topk_idx, c, ws), c)
+
+
+@pytest.mark.parametrize("key", SMALL)
+def test_small_shapes_take_the_sweep_and_ignore_a_workspace(key):
+    """Below 4 chunks the size query is 0 and a workspace passed anyway
+    changes nothing: the sweep runs and the results are the oracle's."""
+    c = _case(key)
+    assert _chunks(c) < 4
+    assert moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R) == 0
+    d = DevCase(c)
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
     _check(_run(d.topk_idx, c, ws), c)
 
 
@@ -149,7 +174,7 @@ def test_onepass_graph_replays_with_new_routing():
         assert int(o["st"].item()) == ref["status"]
 
 
-@pytest.mark.parametrize("key", ["throughput", "tiny"])
+@pytest.mark.parametrize("key", ["throughput", "four_chunks"])
 def test_onepass_wait_runs_out_and_reports_timeout(key):
     """A bounded wait of the single-pass layout that runs out raises
     MOEDC_ERR_TIMEOUT (the test hook makes the last block wait for a flag no
