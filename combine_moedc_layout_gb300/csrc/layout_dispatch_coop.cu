@@ -406,18 +406,20 @@ int launch_layout_dispatch_coop(const void* x, const int32_t* topk_idx, int T, i
     cfg.numAttrs = 1;
     clear_stale_error();
 #define MOEDC_COOP_LAUNCH(F, C)                                                                  \
-    (void)cudaLaunchKernelEx(&cfg, moedc::layout_dispatch_coop_kernel<F, C>, xb, topk_idx, T, H, \
-                             K, E, R, cap, ch, num_tokens_per_expert, num_tokens_per_rank,     \
-                             is_token_in_rank, slot, recv, scales, src_idx, bar, counts, host_epoch, \
-                             target, dev_status)
-    if (base == MOEDC_BF16)
-        MOEDC_COOP_LAUNCH(false, false);
-    else if (cols)
-        MOEDC_COOP_LAUNCH(true, true);
-    else
-        MOEDC_COOP_LAUNCH(true, false);
+    cudaLaunchKernelEx(&cfg, moedc::layout_dispatch_coop_kernel<F, C>, xb, topk_idx, T, H,       \
+                       K, E, R, cap, ch, num_tokens_per_expert, num_tokens_per_rank,           \
+                       is_token_in_rank, slot, recv, scales, src_idx, bar, counts, host_epoch,  \
+                       target, dev_status)
+    const cudaError_t err = base == MOEDC_BF16 ? MOEDC_COOP_LAUNCH(false, false)
+                            : cols             ? MOEDC_COOP_LAUNCH(true, true)
+                                               : MOEDC_COOP_LAUNCH(true, false);
 #undef MOEDC_COOP_LAUNCH
-    return launch_status();
+    if (err == cudaErrorCooperativeLaunchTooLarge) {
+        // fewer SMs than the device reports (a partitioned GPU): two launches instead
+        clear_stale_error();
+        return MOEDC_ERR_UNIMPLEMENTED;
+    }
+    return err == cudaSuccess ? MOEDC_OK : MOEDC_ERR_CUDA;
 }
 
 }  // namespace moedc_host

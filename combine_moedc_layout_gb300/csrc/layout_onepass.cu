@@ -42,6 +42,7 @@
 #include <atomic>
 #include <chrono>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -365,6 +366,26 @@ size_t op_smem_bytes(int E, int R)
            sizeof(int32_t);
 }
 
+constexpr int kOpMaxDevices = 64;
+std::mutex g_op_smem_mutex;
+bool g_op_smem_set[kOpMaxDevices] = {};
+
+bool op_smem_ready()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kOpMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_op_smem_mutex);
+    if (g_op_smem_set[dev]) return true;
+    if (cudaFuncSetAttribute((const void*)moedc::layout_onepass_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)op_smem_bytes(MOEDC_MAX_E, MOEDC_MAX_E)) != cudaSuccess) {
+        clear_stale_error();
+        return false;
+    }
+    g_op_smem_set[dev] = true;
+    return true;
+}
+
 }  // namespace
 
 // Workspace of the single-pass layout: the generation word (in a 256-byte
@@ -393,17 +414,8 @@ int launch_layout_onepass(const int32_t* topk_idx, int T, int K, int E, int R, i
     const int chunks = T > 0 ? (T + tpc - 1) / tpc : 1;
     const size_t sm = op_smem_bytes(E, R);
     // dynamic shared memory beyond the default 48 KB needs the kernel's limit
-    // raised; raised once to the largest size met so far
-    static std::atomic<size_t> g_smem_limit{48 * 1024};
-    if (sm > g_smem_limit.load(std::memory_order_relaxed)) {
-        if (cudaFuncSetAttribute((const void*)moedc::layout_onepass_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
-            cudaSuccess) {
-            clear_stale_error();
-            return MOEDC_ERR_UNIMPLEMENTED;
-        }
-        g_smem_limit.store(sm, std::memory_order_relaxed);
-    }
+    // raised: once per device, to the largest size any shape needs
+    if (sm > 48 * 1024 && !op_smem_ready()) return MOEDC_ERR_UNIMPLEMENTED;
     // the waits need every chunk's block resident at once
     if (chunks > resident_blocks((const void*)moedc::layout_onepass_kernel, moedc::kOpThreads,
                                  sm))
@@ -428,10 +440,15 @@ int launch_layout_onepass(const int32_t* topk_idx, int T, int K, int E, int R, i
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     clear_stale_error();
-    (void)cudaLaunchKernelEx(&cfg, moedc::layout_onepass_kernel, topk_idx, T, K, E, R, cap, tpc,
-                             num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, slot,
-                             gen, rows, host_epoch, extra, dev_status);
-    return launch_status();
+    const cudaError_t err = cudaLaunchKernelEx(
+        &cfg, moedc::layout_onepass_kernel, topk_idx, T, K, E, R, cap, tpc, num_tokens_per_expert,
+        num_tokens_per_rank, is_token_in_rank, slot, gen, rows, host_epoch, extra, dev_status);
+    if (err == cudaErrorCooperativeLaunchTooLarge) {
+        // fewer SMs than the device reports (a partitioned GPU): the sweep runs instead
+        clear_stale_error();
+        return MOEDC_ERR_UNIMPLEMENTED;
+    }
+    return err == cudaSuccess ? MOEDC_OK : MOEDC_ERR_CUDA;
 }
 
 }  // namespace moedc_host

@@ -192,3 +192,36 @@ def test_onepass_wait_runs_out_and_reports_timeout(key):
         lib.moedc_test_set_wait_extra(0)
     assert int(o["st"].item()) == moedc.ERR_TIMEOUT
     _check(_run(d.topk_idx, c, ws), c)
+
+
+def _status_case(kind):
+    c = synth.make_random_case(60, T=2000, H=8, K=6, E=24, R=4, cap=None, dtype=synth.BF16,
+                               mask_p=0.03)
+    assert _chunks(c) >= 4
+    if kind in ("capacity", "both"):
+        c.cap = max(1, c.cap - 15)                 # the fullest experts overflow
+    if kind in ("range", "both"):
+        c.topk_idx[0, 2] = c.E                     # first chunk
+        c.topk_idx[c.T // 2, 0] = -9               # a middle chunk
+        c.topk_idx[c.T - 1, c.K - 1] = 10 ** 6     # the last chunk
+    return c
+
+
+@pytest.mark.parametrize("kind", ["capacity", "range", "both"])
+@pytest.mark.parametrize("path", ["onepass", "sweep"])
+def test_status_codes_match_oracle(kind, path):
+    """Capacity overflow and out-of-range ids spread over several chunks: the
+    device status is the oracle's (the larger code when both occur), counts
+    keep counting past cap, and out-of-range entries get slot -1."""
+    c = _status_case(kind)
+    d = DevCase(c)
+    ws = None
+    if path == "onepass":
+        ws = torch.empty(moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R), dtype=torch.uint8,
+                         device="cuda")
+    o = _run(d.topk_idx, c, ws)
+    ref = oracle.layout(c.topk_idx, c.E, c.R, c.cap)
+    expect = {"capacity": oracle.ERR_CAPACITY, "range": oracle.ERR_EXPERT_RANGE,
+              "both": oracle.ERR_EXPERT_RANGE}[kind]
+    assert ref["status"] == expect
+    _check(o, c)
