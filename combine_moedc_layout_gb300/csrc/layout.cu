@@ -378,19 +378,22 @@ int launch_layout(const int32_t* topk_idx, int T, int K, int E, int R, int cap,
                   size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream)
 {
     const LayoutGeom g = layout_geometry(T, K, E, R);
+    // the single pass, wherever the shape and the workspace allow it
+    const int st = launch_layout_onepass(topk_idx, T, K, E, R, cap, num_tokens_per_expert,
+                                         num_tokens_per_rank, is_token_in_rank, slot, workspace,
+                                         workspace_bytes, dev_status, stream);
+    if (st != MOEDC_ERR_UNIMPLEMENTED) return st;
     if (g.sweep) {
-        const int st = launch_layout_onepass(topk_idx, T, K, E, R, cap, num_tokens_per_expert,
-                                             num_tokens_per_rank, is_token_in_rank, slot,
-                                             workspace, workspace_bytes, dev_status, stream);
-        if (st != MOEDC_ERR_UNIMPLEMENTED) return st;
         const bool vec_ok = aligned(topk_idx, 16);
         clear_stale_error();
         launch(moedc::layout_sweep_kernel, g.blocks, moedc::kSweepThreads, 0, stream, topk_idx, T, K, E, R, cap, vec_ok, num_tokens_per_expert, num_tokens_per_rank,
             is_token_in_rank, slot, dev_status);
         return launch_status();
     }
+    // the two-kernel path (also the fallback of a refused single pass) needs its own scratch
+    if (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)) return MOEDC_ERR_ARG;
     int32_t* ws_hist = static_cast<int32_t*>(workspace);
-    int32_t* ws_rank = ws_hist ? ws_hist + (size_t)g.blocks * E : nullptr;
+    int32_t* ws_rank = ws_hist + (size_t)g.blocks * E;
     if (g.blocks > 1) {
         const size_t sm = moedc::count_smem(g.tpc, K, E, R);
         if (ensure_smem_attr((const void*)moedc::layout_count_kernel, sm) != MOEDC_OK)
@@ -430,9 +433,13 @@ extern "C" int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int R,
     if (!aligned(topk_idx, 4) || !aligned(slot, 4) || !aligned(num_tokens_per_expert, 4) ||
         !aligned(num_tokens_per_rank, 4) || !aligned(dev_status, 4))
         return MOEDC_ERR_ARG;
+    // beyond 65536 entries a workspace is required: one that holds either the
+    // single-pass layout's rows or the two-kernel path's counts
     const LayoutGeom g = layout_geometry(T, K, E, R);
-    if (g.ws > 0 && (!workspace || workspace_bytes < g.ws || !aligned(workspace, 16)))
-        return MOEDC_ERR_ARG;
+    const size_t fast = layout_onepass_workspace_bytes(T, K, E, R);
+    const bool ws_ok = workspace && aligned(workspace, 16) &&
+                       (workspace_bytes >= g.ws || (fast > 0 && workspace_bytes >= fast));
+    if (g.ws > 0 && !ws_ok) return MOEDC_ERR_ARG;
     return launch_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert, num_tokens_per_rank,
                          is_token_in_rank, slot, workspace, workspace_bytes, dev_status, stream);
 }

@@ -1,5 +1,5 @@
 // Routing layout in one pass over the routing table (from 4 chunks of 1024
-// entries up to 65536 entries, with a caller workspace).
+// entries up to 144 chunks of 4096 entries, with a caller workspace).
 //
 // Sources: UCCL PR #749 "[EP] Low-latency mode batch tokens per destination"
 // (code excerpt: per-expert routed-token counters published for the ranks
@@ -9,8 +9,9 @@
 // together).  The layout's outputs are those of layout.cu; only the order of
 // work differs.
 //
-// Block b owns chunk b: a run of whole tokens, at most 1024 (token, k)
-// entries, one entry per thread.
+// Block b owns chunk b: a run of whole tokens, at most 1024 * EPT (token, k)
+// entries, EPT entries per thread (EPT = 1, 2 or 4: the smallest that keeps
+// the chunks within one resident grid).
 //   1. load the chunk's expert ids (one coalesced load);
 //   2. rank each entry among the chunk's entries of the same expert in
 //      (t, k) order: in-warp rank from the ballot match of the 32-entry tile,
@@ -50,14 +51,10 @@ namespace moedc {
 
 constexpr int kOpThreads = 1024;
 constexpr int kOpWarps = kOpThreads / kWarp;
-// routing entries per thread: a chunk holds 1024 * kOpEntriesPerThread
-// entries, a warp kOpEntriesPerThread consecutive 32-entry tiles
-#ifndef MOEDC_OP_EPT
-#define MOEDC_OP_EPT 1
-#endif
-constexpr int kOpEntriesPerThread = MOEDC_OP_EPT;
-constexpr int kOpMaxEntries = kOpThreads * kOpEntriesPerThread;   // of one chunk
-constexpr int kOpMaxChunks = 128;
+// At most this many chunks (blocks of 1024 threads, one per SM): the grid
+// must be resident at once, and a device may report more SMs than a
+// partition of it offers (the launch then falls back).
+constexpr int kOpMaxChunks = 144;
 // Fewer chunks than this take the sweep: one or two blocks rank everything
 // serially, while the sweep spreads it over E + R blocks (measured at 1024
 // entries: 9.8 us single pass, 8.2 us sweep).
@@ -108,11 +105,12 @@ __device__ int op_count_when_tagged(const unsigned long long* p, unsigned long l
 //                            conflicts in the column scan)
 //   s_cnt [E + R]            this chunk's counts (experts, then ranks)
 //   s_pre [E + R]            entries / tokens of the chunks before this one
-//   s_ids [kOpMaxEntries]    the chunk's expert ids; later the partial sums
+//   s_ids [1024 * EPT]       the chunk's expert ids; later the partial sums
 //                            of step 4
 // Warp w owns the chunk's entries [w * 32 * EPT, (w + 1) * 32 * EPT), EPT
 // tiles of 32 in order; thread (w, lane) holds entry w * 32 * EPT + 32 u +
 // lane of tile u.
+template <int EPT>
 __global__ void __launch_bounds__(kOpThreads, 1)
 layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E, int R,
                       int cap, int tpc, int32_t* __restrict__ num_tokens_per_expert,
@@ -143,7 +141,6 @@ layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E,
     const int epr = E / R;
 
     // 1. the chunk's ids (in flight while shared memory is cleared) and the epoch
-    constexpr int EPT = kOpEntriesPerThread;
     const int i0 = warp * kWarp * EPT + lane;   // entry of tile 0; tile u adds 32 u
     int e[EPT];
 #pragma unroll
@@ -358,12 +355,40 @@ std::atomic<unsigned long long> g_op_epoch{
     (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() *
     0xD1B54A32D192ED03ull};
 
-int op_tokens_per_chunk(int K) { return moedc::kOpMaxEntries / K; }
+// entries per thread, tokens per chunk and chunks of a shape, or false when
+// the single pass does not take it (fewer than 4 chunks of 1024 entries: the
+// sweep is faster; more than kOpMaxChunks even at 4 entries per thread)
+struct OpPlan {
+    int ept, tpc, chunks;
+};
 
-size_t op_smem_bytes(int E, int R)
+bool op_plan(int T, int K, OpPlan& p)
 {
-    return ((size_t)moedc::kOpWarps * (E + 1) + 2 * (size_t)(E + R) + moedc::kOpMaxEntries) *
+    if (T < 0 || K < 1) return false;
+    for (int ept = 1; ept <= 4; ept *= 2) {
+        const int tpc = moedc::kOpThreads * ept / K;
+        const int64_t chunks = T > 0 ? ((int64_t)T + tpc - 1) / tpc : 1;
+        if (ept == 1 && chunks < moedc::kOpMinChunks) return false;
+        if (chunks <= moedc::kOpMaxChunks) {
+            p = OpPlan{ept, tpc, (int)chunks};
+            return true;
+        }
+    }
+    return false;
+}
+
+size_t op_smem_bytes(int E, int R, int ept)
+{
+    return ((size_t)moedc::kOpWarps * (E + 1) + 2 * (size_t)(E + R) +
+            (size_t)moedc::kOpThreads * ept) *
            sizeof(int32_t);
+}
+
+const void* op_kernel(int ept)
+{
+    return ept == 1   ? (const void*)moedc::layout_onepass_kernel<1>
+           : ept == 2 ? (const void*)moedc::layout_onepass_kernel<2>
+                      : (const void*)moedc::layout_onepass_kernel<4>;
 }
 
 constexpr int kOpMaxDevices = 64;
@@ -376,11 +401,13 @@ bool op_smem_ready()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kOpMaxDevices) return false;
     std::lock_guard<std::mutex> lock(g_op_smem_mutex);
     if (g_op_smem_set[dev]) return true;
-    if (cudaFuncSetAttribute((const void*)moedc::layout_onepass_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)op_smem_bytes(MOEDC_MAX_E, MOEDC_MAX_E)) != cudaSuccess) {
-        clear_stale_error();
-        return false;
+    for (int ept = 1; ept <= 4; ept *= 2) {
+        if (cudaFuncSetAttribute(op_kernel(ept), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)op_smem_bytes(MOEDC_MAX_E, MOEDC_MAX_E, ept)) !=
+            cudaSuccess) {
+            clear_stale_error();
+            return false;
+        }
     }
     g_op_smem_set[dev] = true;
     return true;
@@ -394,11 +421,9 @@ bool op_smem_ready()
 // this path.
 size_t layout_onepass_workspace_bytes(int T, int K, int E, int R)
 {
-    if ((int64_t)T * K > 65536 || T < 0 || K < 1) return 0;
-    const int tpc = op_tokens_per_chunk(K);
-    const int64_t chunks = T > 0 ? ((int64_t)T + tpc - 1) / tpc : 1;
-    if (chunks > moedc::kOpMaxChunks || chunks < moedc::kOpMinChunks) return 0;
-    return moedc::kOpHeaderBytes + ((size_t)chunks * (E + R) + 2) * sizeof(unsigned long long);
+    OpPlan p;
+    if (!op_plan(T, K, p)) return 0;
+    return moedc::kOpHeaderBytes + ((size_t)p.chunks * (E + R) + 2) * sizeof(unsigned long long);
 }
 
 // MOEDC_ERR_UNIMPLEMENTED when the shape or the workspace does not take this path.
@@ -410,15 +435,16 @@ int launch_layout_onepass(const int32_t* topk_idx, int T, int K, int E, int R, i
     const size_t need = layout_onepass_workspace_bytes(T, K, E, R);
     if (need == 0 || !workspace || workspace_bytes < need || !aligned(workspace, 16))
         return MOEDC_ERR_UNIMPLEMENTED;
-    const int tpc = op_tokens_per_chunk(K);
-    const int chunks = T > 0 ? (T + tpc - 1) / tpc : 1;
-    const size_t sm = op_smem_bytes(E, R);
+    OpPlan plan;
+    if (!op_plan(T, K, plan)) return MOEDC_ERR_UNIMPLEMENTED;
+    const int tpc = plan.tpc;
+    const int chunks = plan.chunks;
+    const size_t sm = op_smem_bytes(E, R, plan.ept);
     // dynamic shared memory beyond the default 48 KB needs the kernel's limit
     // raised: once per device, to the largest size any shape needs
     if (sm > 48 * 1024 && !op_smem_ready()) return MOEDC_ERR_UNIMPLEMENTED;
     // the waits need every chunk's block resident at once
-    if (chunks > resident_blocks((const void*)moedc::layout_onepass_kernel, moedc::kOpThreads,
-                                 sm))
+    if (chunks > resident_blocks(op_kernel(plan.ept), moedc::kOpThreads, sm))
         return MOEDC_ERR_UNIMPLEMENTED;
 
     char* ws = static_cast<char*>(workspace);
@@ -440,11 +466,17 @@ int launch_layout_onepass(const int32_t* topk_idx, int T, int K, int E, int R, i
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     clear_stale_error();
-    const cudaError_t err = cudaLaunchKernelEx(
-        &cfg, moedc::layout_onepass_kernel, topk_idx, T, K, E, R, cap, tpc, num_tokens_per_expert,
-        num_tokens_per_rank, is_token_in_rank, slot, gen, rows, host_epoch, extra, dev_status);
+#define MOEDC_OP_LAUNCH(P)                                                                      \
+    cudaLaunchKernelEx(&cfg, moedc::layout_onepass_kernel<P>, topk_idx, T, K, E, R, cap, tpc,  \
+                       num_tokens_per_expert, num_tokens_per_rank, is_token_in_rank, slot, gen, \
+                       rows, host_epoch, extra, dev_status)
+    const cudaError_t err = plan.ept == 1   ? MOEDC_OP_LAUNCH(1)
+                            : plan.ept == 2 ? MOEDC_OP_LAUNCH(2)
+                                            : MOEDC_OP_LAUNCH(4);
+#undef MOEDC_OP_LAUNCH
     if (err == cudaErrorCooperativeLaunchTooLarge) {
-        // fewer SMs than the device reports (a partitioned GPU): the sweep runs instead
+        // fewer SMs than the device reports (a partitioned GPU): the sweep or the
+        // two-kernel layout runs instead
         clear_stale_error();
         return MOEDC_ERR_UNIMPLEMENTED;
     }

@@ -13,7 +13,7 @@
 // Rules for users:
 //  * The array holds MOEDC_STATIC_SCRATCH_BYTES per device and stays resident
 //    on every GPU that loads the library until the process exits.  Shapes
-//    whose scratch need (moedc_layout_workspace_bytes) is larger are
+//    that need more scratch than that on every path that uses scratch are
 //    rejected with MOEDC_ERR_ARG before anything is launched.
 //  * The first call on each device looks up the array's device address
 //    (cudaGetSymbolAddress, with that device current) and caches it; make
@@ -69,8 +69,13 @@ extern "C" int moedc_layout_static_scratch(const int32_t* topk_idx, int T, int K
                                            int32_t* dev_status, cudaStream_t stream)
 {
     if (!moedc_host::layout_args_ok(T, K, E, R, cap)) return MOEDC_ERR_ARG;
-    if (moedc_host::layout_geometry(T, K, E, R).ws > (size_t)MOEDC_STATIC_SCRATCH_BYTES)
-        return MOEDC_ERR_ARG;   // the shape needs more scratch than the static array holds
+    // the shape needs more scratch than the static array holds (on both paths
+    // that use scratch: the single pass and the two-kernel layout)
+    const size_t need = moedc_host::layout_geometry(T, K, E, R).ws;
+    const size_t fast = moedc_host::layout_onepass_workspace_bytes(T, K, E, R);
+    if (need > (size_t)MOEDC_STATIC_SCRATCH_BYTES &&
+        (fast == 0 || fast > (size_t)MOEDC_STATIC_SCRATCH_BYTES))
+        return MOEDC_ERR_ARG;
     void* scratch = nullptr;
     const int st = scratch_address(&scratch);
     if (st != MOEDC_OK) return st;

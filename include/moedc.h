@@ -129,11 +129,13 @@ MOEDC_EXPORT const char* moedc_strerror(int code);
  * initialisation needed) and may reuse it across calls that are ordered on
  * one stream; calls that can run at the same time need workspaces of their
  * own.  Up to T * K = 3072 the layout is one sweep launch that needs no
- * workspace (the query returns 0).  From 3073 to 65536 entries the workspace
- * is optional: with it the layout is a single pass over the routing table
- * (one cooperative launch), without it (NULL) the sweep, with identical
- * results.  Beyond 65536 it is required.  Returns 0 for arguments that the
- * layout would reject.
+ * workspace (the query returns 0).  From 3073 entries the layout is a single
+ * pass over the routing table (one cooperative launch) when it has a
+ * workspace of this size; up to 65536 entries the workspace is optional
+ * (without it, NULL, the sweep runs), beyond 65536 it is required, and there
+ * a smaller workspace that holds the two-kernel layout's counts is also
+ * accepted (that layout then runs).  Results are identical on every path.
+ * Returns 0 for arguments that the layout would reject.
  */
 MOEDC_EXPORT size_t moedc_layout_workspace_bytes(int T, int K, int E, int R);
 
@@ -148,7 +150,8 @@ MOEDC_EXPORT size_t moedc_layout_workspace_bytes(int T, int K, int E, int R);
  *   num_tokens_per_rank[r]  = number of distinct tokens with a 1 in column r.
  * Arguments: T >= 0, 1 <= K <= MOEDC_MAX_K, 1 <= E <= MOEDC_MAX_E,
  * 1 <= R <= E with E % R == 0, cap >= 1.  workspace may be NULL (or smaller
- * than moedc_layout_workspace_bytes()) only when T * K <= 65536.
+ * than moedc_layout_workspace_bytes()) when T * K <= 65536; beyond that it
+ * must hold what one of the two layouts that use it needs (above).
  * Data errors (dev_status): MOEDC_ERR_EXPERT_RANGE, MOEDC_ERR_CAPACITY, and
  * MOEDC_ERR_TIMEOUT if a bounded wait of the single-pass layout gave up (its
  * outputs are then unspecified; the next call starts clean).
@@ -166,8 +169,9 @@ MOEDC_EXPORT int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int 
  * allocator of their own, plugins inside a framework whose memory pool owns
  * the GPU, and serving loops that may not call cudaMalloc after start-up.
  * Same arguments, results and data errors as moedc_layout, except:
- *  - shapes whose moedc_layout_workspace_bytes() exceeds
- *    MOEDC_STATIC_SCRATCH_BYTES return MOEDC_ERR_ARG and launch nothing;
+ *  - shapes beyond 65536 entries whose scratch need exceeds
+ *    MOEDC_STATIC_SCRATCH_BYTES on both layouts that use scratch return
+ *    MOEDC_ERR_ARG and launch nothing (below that the sweep needs none);
  *  - the array (MOEDC_STATIC_SCRATCH_BYTES per device) stays resident on every
  *    GPU that loads the library until the process exits;
  *  - the first call on a device looks up the array's device address and
@@ -310,8 +314,7 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  * With MOEDC_SCALES_PER_TOKEN (a row's scale needs all of its slices) the
  * single launch gives each block whole tokens instead.
  *
- * Beyond the single-launch layout (T * K > 65536, where
- * moedc_layout_workspace_bytes is nonzero), with a workspace of at least
+ * Beyond 65536 entries, with a workspace of at least
  * moedc_layout_dispatch_workspace_bytes(T, K, E, R) bytes, it is also ONE
  * launch, a cooperative one [UCCL749 per-expert counts a rank waits on]:
  * each block ranks and counts a contiguous chunk of tokens; a grid barrier;
@@ -323,10 +326,10 @@ MOEDC_EXPORT int moedc_rank_combine(const void* rank_out, int R, int cap_rank, i
  *
  * Everything else runs as moedc_layout then moedc_dispatch: 1024 < T * K <=
  * 65536 (where that is the faster form), a workspace smaller than
- * moedc_layout_dispatch_workspace_bytes (it must still hold
- * moedc_layout_workspace_bytes), a chunk that would exceed 2048 entries, and
- * MOEDC_SCALES_PER_TOKEN beyond 1024 entries.  Results are identical on every
- * path.
+ * moedc_layout_dispatch_workspace_bytes (when T * K > 65536 it must still hold
+ * the two-kernel layout's counts), a chunk that would exceed
+ * 2048 entries, and MOEDC_SCALES_PER_TOKEN beyond 1024 entries.  Results are
+ * identical on every path.
  *
  * The barriers' bounded waits are tested through moedc_test_set_wait_extra
  * (below), never through the environment.

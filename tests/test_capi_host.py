@@ -57,10 +57,26 @@ def test_version_and_strerror(lib):
 
 def _onepass_bytes(T, K, E, R):
     """Single-pass layout workspace: a 256-byte header (the generation word),
-    then one row of E + R tagged 64-bit counts per chunk of 1024 // K tokens,
-    then two spare words; 0 below 4 chunks, where the sweep runs."""
-    chunks = max(1, -(-T // (1024 // K)))
-    return 256 + (chunks * (E + R) + 2) * 8 if chunks >= 4 else 0
+    then one row of E + R tagged 64-bit counts per chunk, then two spare
+    words.  A chunk holds 1024 * ept // K tokens with the smallest ept in
+    (1, 2, 4) that keeps it to at most 144 chunks; 0 below 4 chunks of 1024
+    entries (the sweep runs) and beyond 144 chunks at ept 4."""
+    for ept in (1, 2, 4):
+        chunks = max(1, -(-T // (1024 * ept // K)))
+        if ept == 1 and chunks < 4:
+            return 0
+        if chunks <= 144:
+            return 256 + (chunks * (E + R) + 2) * 8
+    return 0
+
+
+def _blocked_bytes(T, K, E, R):
+    """The two-kernel layout's counts beyond 65536 entries: blocks of
+    max(ceil(1024 / K), ceil(T / 1024)) tokens, (E + R) int32 each."""
+    if T * K <= 65536:
+        return 0
+    tpc = max(-(-1024 // K), -(-T // 1024))
+    return -(-T // tpc) * (E + R) * 4
 
 
 def test_workspace_bytes(lib):
@@ -75,9 +91,20 @@ def test_workspace_bytes(lib):
     assert moedc.moedc_layout_workspace_bytes(8192, 8, 256, 8) == _onepass_bytes(8192, 8, 256, 8)
     assert moedc.moedc_layout_workspace_bytes(2048, 32, 1024, 1024) == \
         _onepass_bytes(2048, 32, 1024, 1024)
-    # beyond: 128 tokens per block -> blocks x (E + R) int32
-    assert moedc.moedc_layout_workspace_bytes(8193, 8, 256, 8) == 65 * (256 + 8) * 4
+    # beyond 65536 entries: the larger of the single-pass rows and the
+    # two-kernel layout's counts (blocks x (E + R) int32)
+    assert _blocked_bytes(8193, 8, 256, 8) == 65 * (256 + 8) * 4
+    assert _onepass_bytes(8193, 8, 256, 8) == 256 + (65 * 264 + 2) * 8
+    assert moedc.moedc_layout_workspace_bytes(8193, 8, 256, 8) == 256 + (65 * 264 + 2) * 8
+    assert _blocked_bytes(40000, 8, 128, 8) == 313 * (128 + 8) * 4
+    assert _onepass_bytes(40000, 8, 128, 8) == 256 + (79 * 136 + 2) * 8     # 4 per thread
     assert moedc.moedc_layout_workspace_bytes(40000, 8, 128, 8) == 313 * (128 + 8) * 4
+    assert _onepass_bytes(20000, 8, 128, 8) == 256 + (79 * 136 + 2) * 8     # 2 per thread
+    for shape in [(12000, 8, 256, 8), (20000, 8, 128, 8), (90000, 6, 60, 6), (120000, 6, 60, 6),
+                  (16384, 8, 1024, 1024)]:
+        assert moedc.moedc_layout_workspace_bytes(*shape) == max(_onepass_bytes(*shape),
+                                                                 _blocked_bytes(*shape)), shape
+    assert _onepass_bytes(120000, 6, 60, 6) == 0          # beyond 144 chunks of 4096 entries
     # the one-call layout+dispatch: the layout's workspace while the layout
     # is one launch (fused block, or layout then dispatch), beyond it the
     # cooperative launch's barrier words and count rows [E + R][2048]

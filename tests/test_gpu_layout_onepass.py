@@ -225,3 +225,54 @@ def test_status_codes_match_oracle(kind, path):
               "both": oracle.ERR_EXPERT_RANGE}[kind]
     assert ref["status"] == expect
     _check(o, c)
+
+
+# beyond 65536 entries: the single pass at 1, 2 and 4 entries per thread, and
+# the two-kernel layout (given exactly its own workspace) on the same shapes
+LARGE = {
+    "ept1_96000": dict(seed=70, T=12000, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16,
+                       mask_p=0.02),
+    "ept2_160000": dict(seed=71, T=20000, H=8, K=8, E=128, R=8, cap=None, dtype=synth.BF16),
+    "ept4_320000": dict(seed=72, T=40000, H=8, K=8, E=128, R=8, cap=None, dtype=synth.BF16,
+                        mask_p=0.01),
+    "ept4_540000": dict(seed=73, T=90000, H=8, K=6, E=60, R=6, cap=None, dtype=synth.BF16,
+                        mask_p=0.05),
+    "beyond_720000": dict(seed=74, T=120000, H=8, K=6, E=60, R=6, cap=None, dtype=synth.BF16),
+}
+
+
+def _blocked_bytes(T, K, E, R):
+    tpc = max(-(-1024 // K), -(-T // 1024))
+    return -(-T // tpc) * (E + R) * 4
+
+
+@pytest.mark.parametrize("key", list(LARGE))
+@pytest.mark.parametrize("ws_size", ["query", "two_kernel"])
+def test_large_layouts_match_oracle(key, ws_size):
+    """With the queried workspace the single pass runs (the two-kernel layout
+    beyond 144 chunks); with exactly the two-kernel layout's size that layout
+    runs wherever it needs less than the single pass (96000 and 160000
+    entries here)."""
+    c = synth.make_random_case(**LARGE[key])
+    assert c.T * c.K > 65536
+    d = DevCase(c)
+    n = moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R) if ws_size == "query" else \
+        _blocked_bytes(c.T, c.K, c.E, c.R)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    _check(_run(d.topk_idx, c, ws), c)
+
+
+def test_large_single_pass_wait_runs_out_and_reports_timeout():
+    c = synth.make_random_case(**LARGE["ept4_320000"])
+    d = DevCase(c)
+    ws = torch.empty(moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R), dtype=torch.uint8,
+                     device="cuda")
+    lib = moedc.load()
+    lib.moedc_test_set_wait_extra(1)
+    try:
+        o = _run(d.topk_idx, c, ws)
+        torch.cuda.synchronize()
+    finally:
+        lib.moedc_test_set_wait_extra(0)
+    assert int(o["st"].item()) == moedc.ERR_TIMEOUT
+    _check(_run(d.topk_idx, c, ws), c)
