@@ -14,11 +14,12 @@
 // the chunks within one resident grid).
 //   1. load the chunk's expert ids (one coalesced load);
 //   2. rank each entry among the chunk's entries of the same expert in
-//      (t, k) order: in-warp rank from the ballot match of the 32-entry tile,
-//      plus the counts of the earlier warps (a shuffle scan over the 32 warp
-//      counts of each expert), giving the chunk's per-expert totals; the
-//      chunk's token-in-rank rows, and per rank the number of its tokens
-//      that reach it;
+//      (t, k) order: in-warp rank from the ballot match of each 32-entry tile
+//      (with EPT > 1 plus the warp's running count of the expert), plus the
+//      counts of the earlier warps (a scan over the 32 warp counts of each
+//      expert), giving the chunk's per-expert totals; the chunk's
+//      token-in-rank rows, and per rank the number of its tokens that reach
+//      it;
 //   3. publish those E + R counts as row b of the workspace, each count in a
 //      64-bit word whose upper bits carry this launch's epoch, so that a word
 //      is its own flag (no fence, no separate flag);
