@@ -254,3 +254,34 @@ def test_plain_c_caller_compiles_and_links(lib, tmp_path):
     with no C++ or Python in between (running it needs a GPU: see
     test_gpu_capi_c.py)."""
     assert os.path.exists(_build_c_caller(tmp_path))
+
+
+def test_bench_threaded_oracle_step_matches_single_thread():
+    """The all-cores CPU baseline splits dispatch and combine by token runs over
+    threads; its outputs must equal the single-threaded oracle step bit for
+    bit (the bench asserts the same on the full workload)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import bench
+    from combine_moedc_layout_gb300 import synth
+    c = synth.make_case("throughput")
+    c.extra["eo_host"] = synth.make_expert_out(c, 0)
+    assert bench._token_chunks(10, 4) == [(0, 2), (2, 5), (5, 7), (7, 10)]
+    assert bench._token_chunks(3, 8) == [(0, 1), (1, 2), (2, 3)]
+    _, b1, one = bench.oracle_step(c, 96, keep=True)
+    with ThreadPoolExecutor(max_workers=4) as pool:
+        _, b4, four = bench.oracle_step(c, 96, threads=4, pool=pool, keep=True)
+    assert b1 == b4
+    assert bench.same_oracle_outputs(one, four)
+    four["y"][0, 0] ^= 1                       # a planted difference is caught
+    assert not bench.same_oracle_outputs(one, four)
+
+
+def test_bench_arms_share_one_config_and_report_the_cpu():
+    import bench
+    from combine_moedc_layout_gb300 import synth
+    c = synth.make_case("throughput")
+    a, b = bench.workload_config(c, 1), bench.workload_config(c, 1)
+    assert a == b and {"workload", "T", "H", "K", "E", "R", "cap", "parallelism", "l2"} <= set(a)
+    assert bench.host_cores() >= 1
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
