@@ -276,3 +276,33 @@ def test_large_single_pass_wait_runs_out_and_reports_timeout():
         lib.moedc_test_set_wait_extra(0)
     assert int(o["st"].item()) == moedc.ERR_TIMEOUT
     _check(_run(d.topk_idx, c, ws), c)
+
+
+def test_single_pass_fuzz_back_to_back_on_one_workspace():
+    """40 random shapes (1, 2 and 4 entries per thread, 4 to 144 chunks, masks,
+    duplicates, skewed expert counts) run back to back on one workspace that
+    is never cleared, each checked against the oracle: every call must see
+    only its own epoch's words, whatever the earlier calls left."""
+    rng = np.random.default_rng(2024)
+    shapes = []
+    for i in range(40):
+        R = int(rng.choice([1, 2, 4, 8, 16]))
+        E = R * int(rng.integers(1, 33))
+        K = int(rng.integers(1, min(E, 10) + 1))
+        n = int(rng.integers(3073, 560000))
+        T = max(1, n // K)
+        shapes.append(dict(seed=500 + i, T=T, H=8, K=K, E=E, R=R, cap=None, dtype=synth.BF16,
+                           mask_p=float(rng.choice([0.0, 0.1])),
+                           distinct=bool(rng.integers(0, 2)) and K <= E))
+    cases = [synth.make_random_case(**sh) for sh in shapes]
+    sizes = [moedc.moedc_layout_workspace_bytes(c.T, c.K, c.E, c.R) for c in cases]
+    ws = torch.empty(max(sizes), dtype=torch.uint8, device="cuda")
+    ran_single_pass = 0
+    for c, n in zip(cases, sizes):
+        o = _outputs(c.T, c.K, c.E, c.R)
+        idx = torch.from_numpy(c.topk_idx).cuda()
+        assert moedc.moedc_layout(idx, c.T, c.K, c.E, c.R, c.cap, o["cnt"], o["rk"], o["inr"],
+                                  o["slot"], ws, ws.numel(), o["st"]) == moedc.OK
+        _check(o, c)
+        ran_single_pass += 1 if n > 0 else 0
+    assert ran_single_pass >= 30
