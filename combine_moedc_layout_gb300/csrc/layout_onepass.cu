@@ -188,8 +188,9 @@ layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E,
         uint8_t* inr = is_token_in_rank + (int64_t)t0 * R;
         const bool same_rank = (kOpThreads % R) == 0;
         int mine = 0;
+        const int rshift = (R & (R - 1)) == 0 ? __ffs(R) - 1 : -1;   // R a power of two
         for (int p = tid; p < nt * R; p += kOpThreads) {
-            const int tl = p / R;
+            const int tl = rshift >= 0 ? p >> rshift : p / R;
             const int rr = p - tl * R;
             const bool in = op_token_in_rank(s_ids + tl * K, K, rr * epr, epr);
             inr[p] = in ? 1 : 0;
