@@ -15,9 +15,10 @@
 //    on every GPU that loads the library until the process exits.  Shapes
 //    that need more scratch than that on every path that uses scratch are
 //    rejected with MOEDC_ERR_ARG before anything is launched.
-//  * The first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current) and caches it; make
-//    that first call before any stream capture begins.
+//  * The first call on each device that uses scratch looks up the array's
+//    device address (cudaGetSymbolAddress, with that device current) and
+//    caches it; make that first call before any stream capture begins.
+//    Shapes the sweep takes (no workspace asked for) look nothing up.
 //  * Every call in the process shares the one array.  Calls whose kernels
 //    overlap on the GPU (different streams, or different host threads without
 //    ordering) race on it and give wrong slots; order them on one stream.
@@ -76,6 +77,10 @@ extern "C" int moedc_layout_static_scratch(const int32_t* topk_idx, int T, int K
     if (need > (size_t)MOEDC_STATIC_SCRATCH_BYTES &&
         (fast == 0 || fast > (size_t)MOEDC_STATIC_SCRATCH_BYTES))
         return MOEDC_ERR_ARG;
+    if (need == 0 && fast == 0)   // the sweep: no scratch, so no address lookup either
+        return moedc_layout(topk_idx, T, K, E, R, cap, num_tokens_per_expert,
+                            num_tokens_per_rank, is_token_in_rank, slot, nullptr, 0, dev_status,
+                            stream);
     void* scratch = nullptr;
     const int st = scratch_address(&scratch);
     if (st != MOEDC_OK) return st;

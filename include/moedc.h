@@ -128,10 +128,10 @@ MOEDC_EXPORT const char* moedc_strerror(int code);
  * it (any 16-byte aligned device buffer of at least this size, no
  * initialisation needed) and may reuse it across calls that are ordered on
  * one stream; calls that can run at the same time need workspaces of their
- * own.  Up to T * K = 3072 the layout is one sweep launch that needs no
- * workspace (the query returns 0).  From 3073 entries the layout is a single
- * pass over the routing table (one cooperative launch) when it has a
- * workspace of this size; up to 65536 entries the workspace is optional
+ * own.  Up to T = 3 * floor(1024 / K) tokens (T * K = 3072 when K divides
+ * 1024) the layout is one sweep launch that needs no workspace (the query
+ * returns 0).  Beyond that it is a single pass over the routing table (one
+ * cooperative launch) when it has a workspace of this size; up to 65536 entries the workspace is optional
  * (without it, NULL, the sweep runs), beyond 65536 it is required, and there
  * a smaller workspace that holds the two-kernel layout's counts is also
  * accepted (that layout then runs).  Results are identical on every path.
@@ -174,7 +174,8 @@ MOEDC_EXPORT int moedc_layout(const int32_t* topk_idx, int T, int K, int E, int 
  *    MOEDC_ERR_ARG and launch nothing (below that the sweep needs none);
  *  - the array (MOEDC_STATIC_SCRATCH_BYTES per device) stays resident on every
  *    GPU that loads the library until the process exits;
- *  - the first call on a device looks up the array's device address and
+ *  - the first call on a device that uses the array (any shape for which
+ *    moedc_layout_workspace_bytes is not 0) looks up its device address and
  *    caches it; make that first call before any stream capture begins;
  *  - all calls share the array, so calls that overlap on the GPU race and
  *    give wrong results: order them on one stream;

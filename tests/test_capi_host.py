@@ -85,6 +85,13 @@ def test_workspace_bytes(lib):
     assert moedc.moedc_layout_workspace_bytes(128, 8, 288, 8) == 0
     assert moedc.moedc_layout_workspace_bytes(384, 8, 256, 8) == 0
     assert moedc.moedc_layout_workspace_bytes(0, 8, 256, 8) == 0
+    # a chunk holds floor(1024 / K) tokens, so where K does not divide 1024
+    # the single pass starts a little below 3072 entries
+    for T, K, first in [(510, 6, False), (511, 6, True), (1023, 3, False), (1024, 3, True),
+                        (612, 5, False), (613, 5, True), (438, 7, False), (439, 7, True)]:
+        got = moedc.moedc_layout_workspace_bytes(T, K, 42, 6)
+        assert got == _onepass_bytes(T, K, 42, 6), (T, K)
+        assert (got > 0) == first, (T, K, got)
     # from 4 chunks to 65536 entries: the single-pass layout's (optional) workspace
     assert moedc.moedc_layout_workspace_bytes(512, 8, 256, 8) == _onepass_bytes(512, 8, 256, 8) > 0
     assert moedc.moedc_layout_workspace_bytes(4096, 8, 256, 8) == 256 + (32 * 264 + 2) * 8
