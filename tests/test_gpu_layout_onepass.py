@@ -35,6 +35,13 @@ RANDOM = {
                                dtype=synth.BF16),
     "k3_ragged": dict(seed=40, T=21845, H=8, K=3, E=48, R=6, cap=None, dtype=synth.BF16,
                       mask_p=0.3),
+    # token-in-rank from shuffles (K a power of two, R <= K): one rank, fewer
+    # ranks than K, two entries per token with repeats
+    "k4_r1": dict(seed=43, T=3000, H=8, K=4, E=12, R=1, cap=None, dtype=synth.BF16, mask_p=0.1),
+    "k16_r4": dict(seed=44, T=2000, H=8, K=16, E=64, R=4, cap=None, dtype=synth.BF16,
+                   mask_p=0.05),
+    "k2_r2": dict(seed=45, T=9000, H=8, K=2, E=10, R=2, cap=None, dtype=synth.BF16,
+                  distinct=False),
 }
 
 
@@ -238,6 +245,8 @@ LARGE = {
     "ept4_540000": dict(seed=73, T=90000, H=8, K=6, E=60, R=6, cap=None, dtype=synth.BF16,
                         mask_p=0.05),
     "beyond_720000": dict(seed=74, T=120000, H=8, K=6, E=60, R=6, cap=None, dtype=synth.BF16),
+    "ept2_k2_160000": dict(seed=75, T=80000, H=8, K=2, E=10, R=2, cap=None, dtype=synth.BF16,
+                           mask_p=0.05),
 }
 
 
