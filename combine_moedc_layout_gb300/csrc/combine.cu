@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kCombineThreads, MOEDC_COMBINE_MINB)
 combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
                const float* __restrict__ topk_weights, int T, int K,
-               uint16_t* __restrict__ y, int32_t* __restrict__ status)
+               uint16_t* __restrict__ y, int32_t* __restrict__ status, float neg_zero)
 {
     pdl_enter();
     const int lane = threadIdx.x % kWarp;
@@ -107,7 +107,7 @@ combine_kernel(const uint16_t* __restrict__ expert_out, int E, int cap, int H,
                     const uint32_t u[4] = {buf[j][v].x, buf[j][v].y, buf[j][v].z, buf[j][v].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)   // acc + w * x, each rounded, never fused
-                        acc[4 * v + i] = add2_rn(acc[4 * v + i], mul2_rn(w2, bf16x2_to_f32x2(u[i])));
+                        acc[4 * v + i] = acc_prod2_rn(acc[4 * v + i], w2, bf16x2_to_f32x2(u[i]), neg_zero);
                 }
             }
         }
@@ -154,7 +154,7 @@ extern "C" int moedc_combine(const void* expert_out, int E, int cap, int H,
     if (blocks > resident) blocks = resident;
     clear_stale_error();
     launch(moedc::combine_kernel, (int)blocks, moedc::kCombineThreads, 0, stream, static_cast<const uint16_t*>(expert_out), E, cap, H, topk_idx, slot, topk_weights, T, K,
-        static_cast<uint16_t*>(y), dev_status);
+        static_cast<uint16_t*>(y), dev_status, -0.0f);
     return launch_status();
 }
 
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kCombineThreads, 2)
 combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restrict__ scales,
                     int scale_mode, int E, int cap, int H, const int32_t* __restrict__ topk_idx,
                     const int32_t* __restrict__ slot, const float* __restrict__ topk_weights,
-                    int T, int K, uint16_t* __restrict__ y, int32_t* __restrict__ status)
+                    int T, int K, uint16_t* __restrict__ y, int32_t* __restrict__ status, float neg_zero)
 {
     pdl_enter();
     const int lane = threadIdx.x % kWarp;
@@ -225,8 +225,8 @@ combine_e4m3_kernel(const uint8_t* __restrict__ expert_out, const float* __restr
                     // acc + w * (q * s), each operation rounded, never fused
                     const float2 lo = mul2_rn(e4m3x2_to_f32x2(u[i] & 0xffffu), s2);
                     const float2 hi = mul2_rn(e4m3x2_to_f32x2(u[i] >> 16), s2);
-                    acc[2 * i] = add2_rn(acc[2 * i], mul2_rn(w2, lo));
-                    acc[2 * i + 1] = add2_rn(acc[2 * i + 1], mul2_rn(w2, hi));
+                    acc[2 * i] = acc_prod2_rn(acc[2 * i], w2, lo, neg_zero);
+                    acc[2 * i + 1] = acc_prod2_rn(acc[2 * i + 1], w2, hi, neg_zero);
                 }
             }
         }
@@ -263,7 +263,7 @@ combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __
                          int scale_mode, int E, int cap, int H,
                          const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot,
                          const float* __restrict__ topk_weights, int T, int K,
-                         uint16_t* __restrict__ y, int32_t* __restrict__ status)
+                         uint16_t* __restrict__ y, int32_t* __restrict__ status, float neg_zero)
 {
     pdl_enter();
     const int lane = threadIdx.x % kWarp;
@@ -331,8 +331,8 @@ combine_e4m3_rows_kernel(const uint8_t* __restrict__ expert_out, const float* __
                     // acc + w * (q * s), each operation rounded, never fused
                     const float2 lo = mul2_rn(e4m3x2_to_f32x2(u[i] & 0xffffu), s2);
                     const float2 hi = mul2_rn(e4m3x2_to_f32x2(u[i] >> 16), s2);
-                    acc[2 * i] = add2_rn(acc[2 * i], mul2_rn(w2, lo));
-                    acc[2 * i + 1] = add2_rn(acc[2 * i + 1], mul2_rn(w2, hi));
+                    acc[2 * i] = acc_prod2_rn(acc[2 * i], w2, lo, neg_zero);
+                    acc[2 * i + 1] = acc_prod2_rn(acc[2 * i + 1], w2, hi, neg_zero);
                 }
             }
             if (act) {
@@ -382,7 +382,7 @@ extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_sc
         clear_stale_error();
         launch(moedc::combine_e4m3_rows_kernel, (int)blocks, moedc::kCombineThreads, 0, stream,
                static_cast<const uint8_t*>(expert_out), expert_scales, mode, E, cap, H, topk_idx,
-               slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status);
+               slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status, -0.0f);
         return launch_status();
     }
     const int64_t items = (int64_t)T * ((H + 511) / 512);
@@ -393,6 +393,6 @@ extern "C" int moedc_combine_e4m3(const void* expert_out, const float* expert_sc
     if (blocks > resident) blocks = resident;
     clear_stale_error();
     launch(moedc::combine_e4m3_kernel, (int)blocks, moedc::kCombineThreads, 0, stream, static_cast<const uint8_t*>(expert_out), expert_scales, mode, E, cap, H,
-        topk_idx, slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status);
+        topk_idx, slot, topk_weights, T, K, static_cast<uint16_t*>(y), dev_status, -0.0f);
     return launch_status();
 }

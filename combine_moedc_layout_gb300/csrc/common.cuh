@@ -90,8 +90,14 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t two_codes, float& lo, flo
 // method rounds every product before it is summed, so only one of the two
 // may be packed; packed multiplies measured as fast as packed adds (e4m3
 // combine 55.3 us for either, 59.4 us scalar).
+// A product can instead come from a packed FMA whose addend is -0 held in a
+// register (a kernel argument, so the compiler cannot see its value): x + -0
+// is x for every x under round-to-nearest, so the result is the rounded
+// product, and a sum that consumes an FMA's result cannot be contracted with
+// it.  Then the sum may be packed as well.
 // MOEDC_F32X2 selects the form for comparison builds: bit 0 packed
-// multiplies, bit 1 packed adds (3 is the fusing form: not for use).
+// multiplies, bit 1 packed adds (3 is the fusing form: not for use), bit 2
+// weighted products as packed FMAs with a -0 addend and their sums packed.
 #ifndef MOEDC_F32X2
 #define MOEDC_F32X2 1
 #endif
@@ -142,6 +148,27 @@ __device__ __forceinline__ float2 add2_rn_unfed(float2 a, float2 b)
 }
 
 __device__ __forceinline__ float2 splat2(float s) { return make_float2(s, s); }
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(f32x2_bits(a)), "l"(f32x2_bits(b)), "l"(f32x2_bits(c)));
+    return f32x2_from_bits(r);
+}
+
+// acc + RN(w * x) lane by lane, the product rounded before the sum.
+// `neg_zero` is -0.0f passed in at run time (bit 2 of MOEDC_F32X2).
+__device__ __forceinline__ float2 acc_prod2_rn(float2 acc, float2 w, float2 x, float neg_zero)
+{
+#if MOEDC_F32X2 & 4
+    return add2_rn_unfed(acc, fma2_rn(w, x, splat2(neg_zero)));
+#else
+    (void)neg_zero;
+    return add2_rn(acc, mul2_rn(w, x));
+#endif
+}
 
 // the two bf16 values of a 32-bit word (low half first), widened exactly
 __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w)
