@@ -120,6 +120,10 @@ def _same_as_oracle(got, c):
     dict(seed=44, T=12000, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16, mask_p=0.05),
     # the single-pass layout, its scratch in the static array too (4096 tokens)
     dict(seed=45, T=4096, H=8, K=8, E=256, R=8, cap=None, dtype=synth.BF16),
+    # the sweep (1024 entries): no scratch, so no address lookup
+    dict(seed=47, T=128, H=8, K=8, E=288, R=8, cap=None, dtype=synth.BF16, mask_p=0.05),
+    # K = 6: 4 chunks of floor(1024 / 6) tokens at 511 tokens (3066 entries), the single pass
+    dict(seed=48, T=511, H=8, K=6, E=60, R=6, cap=None, dtype=synth.BF16),
 ])
 def test_static_scratch_matches_oracle_directly(shape):
     c = synth.make_random_case(**shape)
