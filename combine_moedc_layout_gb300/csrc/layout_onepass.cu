@@ -183,25 +183,33 @@ layout_onepass_kernel(const int32_t* __restrict__ topk_idx, int T, int K, int E,
     // token-in-rank rows of this chunk, and per rank its tokens that reach it.
     // With K a power of two up to 32, a 32-entry tile holds whole tokens, K
     // lanes each: the token's lanes OR their entries' rank bits by shuffles.
-    // With R <= K as well, lane k of a token owns rank k: it writes that byte
-    // and sums the bit over its tiles, and lanes of equal k sum across the
-    // warp's tokens before one shared-memory add.
-    if (K >= 2 && K <= kWarp && (K & (K - 1)) == 0 && R <= K) {
+    // With R <= 32 as well, the ranks go in rounds of K: in round r0, lane k
+    // of a token owns rank r0 + k: it writes that byte and sums the bit over
+    // its tiles, and lanes of equal k sum across the warp's tokens before one
+    // shared-memory add.
+    if (K >= 2 && K <= kWarp && (K & (K - 1)) == 0 && R <= kWarp) {
         const int kl = lane & (K - 1);
-        int mine = 0;
+        unsigned m[EPT];
 #pragma unroll
         for (int u = 0; u < EPT; ++u) {
-            const int i = i0 + u * kWarp;
-            unsigned m = ((valid_bits >> u) & 1u) ? 1u << (e[u] / epr) : 0u;
-            for (int d = 1; d < K; d <<= 1) m |= __shfl_xor_sync(0xffffffffu, m, d);
-            if (i < n && kl < R) {
-                const int in = (int)((m >> kl) & 1u);
-                is_token_in_rank[((int64_t)t0 + i / K) * R + kl] = (uint8_t)in;
-                mine += in;
-            }
+            m[u] = ((valid_bits >> u) & 1u) ? 1u << (e[u] / epr) : 0u;
+            for (int d = 1; d < K; d <<= 1) m[u] |= __shfl_xor_sync(0xffffffffu, m[u], d);
         }
-        for (int d = K; d < kWarp; d <<= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
-        if (lane < R && mine) atomicAdd(&s_cnt[E + lane], mine);
+        for (int r0 = 0; r0 < R; r0 += K) {
+            const int r = r0 + kl;
+            int mine = 0;
+#pragma unroll
+            for (int u = 0; u < EPT; ++u) {
+                const int i = i0 + u * kWarp;
+                if (i < n && r < R) {
+                    const int in = (int)((m[u] >> r) & 1u);
+                    is_token_in_rank[((int64_t)t0 + i / K) * R + r] = (uint8_t)in;
+                    mine += in;
+                }
+            }
+            for (int d = K; d < kWarp; d <<= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
+            if (lane < K && r < R && mine) atomicAdd(&s_cnt[E + r], mine);
+        }
     } else {
         // Otherwise each thread takes (token, rank) pairs and scans the token's ids
         // in shared memory.  When R divides the block, every pair a thread visits

@@ -42,6 +42,12 @@ RANDOM = {
                    mask_p=0.05),
     "k2_r2": dict(seed=45, T=9000, H=8, K=2, E=10, R=2, cap=None, dtype=synth.BF16,
                   distinct=False),
+    # more ranks than K, in rounds of K ranks: EP16 with top-8, 32 ranks with K = 4 and K = 2
+    "k8_r16": dict(seed=46, T=3000, H=8, K=8, E=128, R=16, cap=None, dtype=synth.BF16,
+                   mask_p=0.05),
+    "k4_r32": dict(seed=47, T=5000, H=8, K=4, E=64, R=32, cap=None, dtype=synth.BF16),
+    "k2_r32": dict(seed=48, T=7000, H=8, K=2, E=96, R=32, cap=None, dtype=synth.BF16,
+                   distinct=False, mask_p=0.1),
 }
 
 
@@ -247,6 +253,8 @@ LARGE = {
     "beyond_720000": dict(seed=74, T=120000, H=8, K=6, E=60, R=6, cap=None, dtype=synth.BF16),
     "ept2_k2_160000": dict(seed=75, T=80000, H=8, K=2, E=10, R=2, cap=None, dtype=synth.BF16,
                            mask_p=0.05),
+    "ept2_r16_160000": dict(seed=76, T=20000, H=8, K=8, E=128, R=16, cap=None,
+                            dtype=synth.BF16),
 }
 
 
