@@ -58,8 +58,8 @@ __device__ __forceinline__ void store_slice_bf16(const SliceX& v, int H, int sli
         const int row = __shfl_sync(0xffffffffu, my_row, k);
         if (row < 0) continue;
         uint16_t* dst = recv + (int64_t)row * H;
-        if (a0) st_global_cs(reinterpret_cast<uint4*>(dst + c0), v.a);
-        if (a1) st_global_cs(reinterpret_cast<uint4*>(dst + c1), v.b);
+        if (a0) st_global_recv(reinterpret_cast<uint4*>(dst + c0), v.a);
+        if (a1) st_global_recv(reinterpret_cast<uint4*>(dst + c1), v.b);
     }
 }
 
@@ -135,10 +135,10 @@ __device__ __forceinline__ void store_slice_fp8(const SliceX& v, int H, int slic
         int64_t sbase = 0;
         if (kScaleCols) sbase = __shfl_sync(0xffffffffu, my_sbase, k);
         if (row < 0 || !act) continue;
-        st_global_cs(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), q);
+        st_global_recv(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), q);
         if (leader) {
             const int64_t si = kScaleCols ? sbase + (int64_t)g * cap : (int64_t)row * G + g;
-            st_global_cs_f32(scales + si, sc);
+            st_global_recv_f32(scales + si, sc);
         }
     }
 }

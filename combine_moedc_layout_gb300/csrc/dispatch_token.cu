@@ -101,12 +101,12 @@ dispatch_token_kernel(const uint16_t* __restrict__ x, int T, int H,
             for (int k = 0; k < K; ++k) {
                 const int row = __shfl_sync(0xffffffffu, my_row, k);
                 if (row >= 0 && act)
-                    st_global_cs(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), q);
+                    st_global_recv(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), q);
             }
         }
         if (warp == 0 && lane < K && my_row >= 0) {
             src_idx[my_row] = t;
-            st_global_cs_f32(scales + my_row, sc);
+            st_global_recv_f32(scales + my_row, sc);
         }
     }
     if (bad) raise_status(status, MOEDC_ERR_EXPERT_RANGE);

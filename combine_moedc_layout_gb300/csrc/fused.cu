@@ -319,13 +319,13 @@ fused_layout_dispatch_token_kernel(const uint16_t* __restrict__ x,
             for (int k = 0; k < K; ++k) {
                 const int row = __shfl_sync(0xffffffffu, my_row, k);
                 if (row >= 0 && c0 < H)
-                    st_global_cs(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), qv);
+                    st_global_recv(reinterpret_cast<uint4*>(recv + (int64_t)row * H + c0), qv);
             }
         }
         if (warp == 0) {
             publish_token(t, lane, K, E, R, cap, s_idx, s_slot, slot, is_token_in_rank, src_idx,
                           status);
-            if (lane < K && my_row >= 0) st_global_cs_f32(scales + my_row, sc);
+            if (lane < K && my_row >= 0) st_global_recv_f32(scales + my_row, sc);
         }
     }
 }
